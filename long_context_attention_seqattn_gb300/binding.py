@@ -1,0 +1,251 @@
+"""ctypes binding of libseqattn (include/seqattn.h): argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+turns torch tensors into device pointers and sizes, passes the current torch
+CUDA stream, and raises ``SeqattnError`` on a non-OK status.  If the library
+has not been built, the first call raises; there is no other code path.
+"""
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+SEQATTN_OK = 0
+SEQATTN_ERR_INVALID_ARG = 1
+SEQATTN_ERR_UNSUPPORTED = 2
+SEQATTN_ERR_CUDA = 3
+SEQATTN_ERR_TIMEOUT = 4
+
+SEQATTN_BF16 = 0
+SEQATTN_FP32 = 1
+
+EXPORTED = (
+    "seqattn_chunk_fwd",
+    "seqattn_chunk_bwd",
+    "seqattn_reset_accum",
+    "seqattn_bwd_workspace_size",
+    "seqattn_sync_status",
+    "seqattn_status_string",
+    "seqattn_last_error",
+)
+
+
+class Problem(ctypes.Structure):
+    """Mirror of ``seqattn_problem``."""
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("seq_capacity", ctypes.c_int64),
+        ("dtype", ctypes.c_int32),
+    ]
+
+
+class SeqattnError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"seqattn status {status}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path=LIB_PATH):
+    """Load libseqattn.so (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run long_context_attention_seqattn_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER(Problem)
+    vp, i64, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.seqattn_chunk_fwd.argtypes = [P, i64, i64, i64, f32, vp, vp, vp, vp, vp, vp]
+    lib.seqattn_chunk_fwd.restype = ctypes.c_int
+    lib.seqattn_chunk_bwd.argtypes = [P, i64, i64, i64, f32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                      vp, sz, vp]
+    lib.seqattn_chunk_bwd.restype = ctypes.c_int
+    lib.seqattn_reset_accum.argtypes = [P, vp, vp, vp]
+    lib.seqattn_reset_accum.restype = ctypes.c_int
+    lib.seqattn_bwd_workspace_size.argtypes = [P, i64]
+    lib.seqattn_bwd_workspace_size.restype = sz
+    lib.seqattn_sync_status.argtypes = [vp]
+    lib.seqattn_sync_status.restype = ctypes.c_int
+    lib.seqattn_status_string.argtypes = [ctypes.c_int]
+    lib.seqattn_status_string.restype = ctypes.c_char_p
+    lib.seqattn_last_error.argtypes = []
+    lib.seqattn_last_error.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(status):
+    if status != SEQATTN_OK:
+        lib = load_library()
+        raise SeqattnError(status, lib.seqattn_last_error().decode())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _dtype_code(dt):
+    if dt == torch.bfloat16:
+        return SEQATTN_BF16
+    if dt == torch.float32:
+        return SEQATTN_FP32
+    raise TypeError(f"unsupported element type {dt}")
+
+
+def problem_for(k, num_q_heads, dtype=None):
+    """seqattn_problem for caches ``k`` of shape [B, T, Hkv, d]."""
+    B, T, Hkv, d = k.shape
+    return Problem(B, num_q_heads, Hkv, d, T, _dtype_code(dtype or k.dtype))
+
+
+def _need(t, name, dtype, shape=None):
+    if not t.is_cuda or not t.is_contiguous() or t.dtype != dtype:
+        raise ValueError(f"{name} must be a contiguous CUDA tensor of {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def chunk_fwd(q, k, v, o, lse, q_start, prefix_len=None, scale=None, stream=None):
+    """Forward of the chunk whose queries ``q`` [B, c, Hq, d] sit at absolute
+    rows [q_start, q_start + c) of the caches ``k``, ``v`` [B, T, Hkv, d].
+    Writes ``o`` [B, c, Hq, d] and ``lse`` [B, Hq, c] (float32)."""
+    B, c, Hq, d = q.shape
+    prefix_len = q_start if prefix_len is None else prefix_len
+    scale = d ** -0.5 if scale is None else scale
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _need(t, name, q.dtype)
+    _need(lse, "lse", torch.float32, (B, Hq, c))
+    pb = problem_for(k, Hq, q.dtype)
+    _check(load_library().seqattn_chunk_fwd(ctypes.byref(pb), q_start, c, prefix_len, scale,
+                                            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                            _stream(stream)))
+
+
+def bwd_workspace_size(k, num_q_heads, q_len, dtype=None):
+    pb = problem_for(k, num_q_heads, dtype)
+    return int(load_library().seqattn_bwd_workspace_size(ctypes.byref(pb), q_len))
+
+
+def chunk_bwd(q, k, v, o, lse, d_o, dq, dk_accum, dv_accum, q_start, prefix_len=None,
+              scale=None, workspace=None, stream=None):
+    """Backward of one chunk: overwrites ``dq`` (float32, shape of q) and adds
+    into ``dk_accum``/``dv_accum`` (float32, shape of k).  ``workspace`` is a
+    uint8 CUDA tensor of at least ``bwd_workspace_size`` bytes (allocated
+    here when omitted)."""
+    B, c, Hq, d = q.shape
+    prefix_len = q_start if prefix_len is None else prefix_len
+    scale = d ** -0.5 if scale is None else scale
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("d_o", d_o)):
+        _need(t, name, q.dtype)
+    _need(lse, "lse", torch.float32, (B, Hq, c))
+    _need(dq, "dq", torch.float32, q.shape)
+    _need(dk_accum, "dk_accum", torch.float32, k.shape)
+    _need(dv_accum, "dv_accum", torch.float32, k.shape)
+    pb = problem_for(k, Hq, q.dtype)
+    lib = load_library()
+    need = int(lib.seqattn_bwd_workspace_size(ctypes.byref(pb), c))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(lib.seqattn_chunk_bwd(ctypes.byref(pb), q_start, c, prefix_len, scale, _ptr(q), _ptr(k),
+                                 _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk_accum),
+                                 _ptr(dv_accum), _ptr(workspace), workspace.numel(),
+                                 _stream(stream)))
+
+
+def reset_accum(dk_accum, dv_accum, num_q_heads=None, stream=None):
+    """Zero the float32 running sums (shape [B, T, Hkv, d])."""
+    _need(dk_accum, "dk_accum", torch.float32)
+    _need(dv_accum, "dv_accum", torch.float32, dk_accum.shape)
+    Hkv = dk_accum.shape[2]
+    pb = problem_for(dk_accum, num_q_heads or Hkv, torch.float32)
+    _check(load_library().seqattn_reset_accum(ctypes.byref(pb), _ptr(dk_accum), _ptr(dv_accum),
+                                              _stream(stream)))
+
+
+def sync_status(stream=None):
+    """Synchronise the stream and raise if a kernel gave up a bounded wait."""
+    _check(load_library().seqattn_sync_status(_stream(stream)))
+
+
+def status_string(code):
+    return load_library().seqattn_status_string(code).decode()
+
+
+# ------------------------------------------------------------------ layer driver
+
+class LayerBuffers:
+    """Device buffers of one layer pass: outputs and accumulators, allocated
+    once and reused across passes."""
+
+    def __init__(self, q, k, chunk):
+        B, T, Hq, d = q.shape
+        dev = q.device
+        self.o = torch.empty_like(q)
+        self.dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        self.dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+        self.dv = torch.empty(k.shape, dtype=torch.float32, device=dev)
+        # per-chunk LSE slices must be contiguous [B, Hq, c]: keep one buffer per chunk
+        self.chunk = chunk
+        self.starts = list(range(0, T, chunk))
+        self.lse_chunks = [torch.empty((B, Hq, min(chunk, T - s)), dtype=torch.float32, device=dev)
+                           for s in self.starts]
+        self.workspace = torch.empty(max(256, bwd_workspace_size(k, Hq, chunk, q.dtype)),
+                                     dtype=torch.uint8, device=dev)
+
+
+def _rows(t, s, e):
+    """Rows [s, e) of a [B, T, H, d] tensor as a contiguous chunk tensor."""
+    v = t[:, s:e]
+    return v if v.is_contiguous() else v.contiguous()
+
+
+def layer_forward_backward(q, k, v, d_o, chunk, scale=None, bufs=None, stream=None,
+                           bwd_order="descending"):
+    """One pass of the chunked layer: reset the running sums, forward chunks
+    0..D-1, backward chunks D-1..0 (SeCO's last-to-first relay order).
+    Returns the LayerBuffers holding O, per-chunk LSE, dQ, dK, dV."""
+    B, T, Hq, d = q.shape
+    if bufs is None:
+        bufs = LayerBuffers(q, k, chunk)
+    reset_accum(bufs.dk, bufs.dv, Hq, stream)
+    for i, s in enumerate(bufs.starts):
+        e = min(s + chunk, T)
+        o_c = bufs.o[:, s:e]
+        if o_c.is_contiguous():
+            chunk_fwd(_rows(q, s, e), k, v, o_c, bufs.lse_chunks[i], s, s, scale, stream)
+        else:
+            tmp = torch.empty_like(o_c.contiguous())
+            chunk_fwd(_rows(q, s, e), k, v, tmp, bufs.lse_chunks[i], s, s, scale, stream)
+            o_c.copy_(tmp)
+    order = list(enumerate(bufs.starts))
+    if bwd_order == "descending":
+        order = order[::-1]
+    for i, s in order:
+        e = min(s + chunk, T)
+        dq_c = bufs.dq[:, s:e]
+        tgt = dq_c if dq_c.is_contiguous() else torch.empty_like(dq_c.contiguous())
+        chunk_bwd(_rows(q, s, e), k, v, _rows(bufs.o, s, e), bufs.lse_chunks[i], _rows(d_o, s, e),
+                  tgt, bufs.dk, bufs.dv, s, s, scale, bufs.workspace, stream)
+        if tgt is not dq_c:
+            dq_c.copy_(tgt)
+    return bufs
+
+
+def gather_lse(bufs):
+    """Concatenate the per-chunk LSE buffers into [B, Hq, T]."""
+    return torch.cat(bufs.lse_chunks, dim=2)

@@ -1,0 +1,51 @@
+// internal.h -- launch plumbing shared between the C-ABI front end and the
+// kernel translation units of libseqattn.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace seqattn {
+
+// Geometry of one chunk call, after validation.
+struct ChunkGeom {
+  int B, Hq, Hkv, G, d;
+  int64_t T;         // cache rows
+  int64_t q_start;   // absolute row of the chunk's first query
+  int64_t q_len;     // rows in the chunk
+  int64_t kv_begin;  // first visible key row (q_start - prefix_len)
+  float scale;       // softmax scale
+};
+
+// ---- float32 exact path (SIMT FMA) ----------------------------------------
+cudaError_t launch_fwd_f32(const ChunkGeom& g, const float* q, const float* k, const float* v,
+                           float* o, float* lse, unsigned int* err, cudaStream_t s);
+cudaError_t launch_bwd_f32(const ChunkGeom& g, const float* q, const float* k, const float* v,
+                           const float* lse, const float* d_o, const float* delta, float* dq,
+                           float* dk, float* dv, unsigned int* err, cudaStream_t s);
+
+// ---- Delta = rowsum(dO o O) (+ zero dq when `zero_dq`), any input type ----
+cudaError_t launch_bwd_prep_bf16(const ChunkGeom& g, const void* o, const void* d_o,
+                                 float* delta, float* dq_to_zero, cudaStream_t s);
+cudaError_t launch_bwd_prep_f32(const ChunkGeom& g, const float* o, const float* d_o,
+                                float* delta, cudaStream_t s);
+
+// ---- zero fill of the float32 accumulators ---------------------------------
+cudaError_t launch_zero_f32(float* a, float* b, int64_t n, cudaStream_t s);
+
+// ---- bf16 tensor-core path (TMA + tcgen05 + TMEM) -------------------------
+// Tensor maps are built by the front end (see tma_maps in seqattn_api.cu).
+struct Bf16FwdMaps {
+  CUtensorMap q, k, v;
+};
+struct Bf16BwdMaps {
+  CUtensorMap q, k, v, d_o;
+};
+cudaError_t launch_fwd_bf16(const ChunkGeom& g, const Bf16FwdMaps& maps, void* o, float* lse,
+                            unsigned int* err, cudaStream_t s);
+cudaError_t launch_bwd_bf16(const ChunkGeom& g, const Bf16BwdMaps& maps, const float* lse,
+                            const float* delta, float* dq, float* dk, float* dv,
+                            unsigned int* err, cudaStream_t s);
+
+}  // namespace seqattn

@@ -1,0 +1,289 @@
+// seqattn_api.cu -- the C ABI declared in include/seqattn.h: argument
+// validation (before any launch), TMA tensor maps, the per-device error word
+// and dispatch to the float32 and bf16 kernel families.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+#include "seqattn.h"
+
+namespace seqattn {
+
+// One error word per device (see sm103_ptx.cuh, "device error word").
+__device__ unsigned int g_seqattn_error_word = 0u;
+
+namespace {
+
+thread_local std::string t_last_error;
+
+seqattn_status fail(seqattn_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+seqattn_status fail(seqattn_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return s;
+}
+
+seqattn_status ok() {
+  t_last_error.clear();
+  return SEQATTN_OK;
+}
+
+seqattn_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(SEQATTN_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_err_ptr[kMaxDevices] = {};
+
+// Device address of this device's error word (looked up once per device).
+cudaError_t error_word(unsigned int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_seqattn_error_word);
+    if (e != cudaSuccess) return e;
+    g_err_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return cudaSuccess;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// 3-D bf16 tensor map over a [rows, heads, d] row-major tensor: box of
+// {64 elements of d, 1 head, box_rows rows}, 128-byte swizzle (one 128-byte
+// row of the box per smem row, the layout the MMA descriptors expect).
+bool make_map(CUtensorMap* m, const void* base, int d, int heads, int64_t rows, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  memset(m, 0, sizeof(*m));
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(heads) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+seqattn_status check_problem(const seqattn_problem* pb) {
+  if (pb == nullptr) return fail(SEQATTN_ERR_INVALID_ARG, "problem is NULL");
+  if (pb->batch < 1 || pb->num_q_heads < 1 || pb->num_kv_heads < 1 || pb->seq_capacity < 1)
+    return fail(SEQATTN_ERR_INVALID_ARG, "batch, heads and seq_capacity must be >= 1");
+  if (pb->num_q_heads % pb->num_kv_heads != 0)
+    return fail(SEQATTN_ERR_INVALID_ARG, "num_q_heads (%d) is not a multiple of num_kv_heads (%d)",
+                pb->num_q_heads, pb->num_kv_heads);
+  if (pb->head_dim != 64 && pb->head_dim != 128)
+    return fail(SEQATTN_ERR_INVALID_ARG, "head_dim %d is not 64 or 128", pb->head_dim);
+  if (pb->dtype != SEQATTN_BF16 && pb->dtype != SEQATTN_FP32)
+    return fail(SEQATTN_ERR_INVALID_ARG, "unknown dtype %d", pb->dtype);
+  if (static_cast<int64_t>(pb->batch) * pb->seq_capacity > INT32_MAX)
+    return fail(SEQATTN_ERR_INVALID_ARG, "batch * seq_capacity exceeds 2^31 - 1 rows");
+  return SEQATTN_OK;
+}
+
+seqattn_status check_chunk(const seqattn_problem* pb, int64_t q_start, int64_t q_len,
+                           int64_t prefix_len, float scale, ChunkGeom* g) {
+  seqattn_status s = check_problem(pb);
+  if (s != SEQATTN_OK) return s;
+  if (q_len < 0) return fail(SEQATTN_ERR_INVALID_ARG, "q_len %lld < 0", (long long)q_len);
+  if (q_start < 0 || prefix_len < 0 || prefix_len > q_start)
+    return fail(SEQATTN_ERR_INVALID_ARG, "need 0 <= prefix_len <= q_start (got %lld, %lld)",
+                (long long)prefix_len, (long long)q_start);
+  if (q_start + q_len > pb->seq_capacity)
+    return fail(SEQATTN_ERR_INVALID_ARG, "q_start + q_len = %lld exceeds seq_capacity %lld",
+                (long long)(q_start + q_len), (long long)pb->seq_capacity);
+  if (!(scale > 0.f) || !isfinite(scale))
+    return fail(SEQATTN_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
+  if (static_cast<int64_t>(pb->batch) * q_len > INT32_MAX)
+    return fail(SEQATTN_ERR_INVALID_ARG, "batch * q_len exceeds 2^31 - 1 rows");
+  if (pb->dtype == SEQATTN_BF16) {
+    if (pb->head_dim != 128)
+      return fail(SEQATTN_ERR_UNSUPPORTED, "bf16 path needs head_dim 128 (got %d)", pb->head_dim);
+    if (q_start % 128 || q_len % 128 || prefix_len % 128)
+      return fail(SEQATTN_ERR_UNSUPPORTED,
+                  "bf16 path needs q_start, q_len and prefix_len to be multiples of 128");
+  }
+  g->B = pb->batch;
+  g->Hq = pb->num_q_heads;
+  g->Hkv = pb->num_kv_heads;
+  g->G = pb->num_q_heads / pb->num_kv_heads;
+  g->d = pb->head_dim;
+  g->T = pb->seq_capacity;
+  g->q_start = q_start;
+  g->q_len = q_len;
+  g->kv_begin = q_start - prefix_len;
+  g->scale = scale;
+  return SEQATTN_OK;
+}
+
+seqattn_status check_ptrs(std::initializer_list<std::pair<const void*, const char*>> ps) {
+  for (auto& p : ps) {
+    if (p.first == nullptr) return fail(SEQATTN_ERR_INVALID_ARG, "%s is NULL", p.second);
+    if (!aligned16(p.first))
+      return fail(SEQATTN_ERR_INVALID_ARG, "%s is not 16-byte aligned", p.second);
+  }
+  return SEQATTN_OK;
+}
+
+size_t workspace_bytes(const seqattn_problem* pb, int64_t q_len) {
+  // Delta [B, Hq, q_len] float32, rounded up to 256 bytes.
+  const size_t delta = static_cast<size_t>(pb->batch) * pb->num_q_heads * q_len * sizeof(float);
+  return (delta + 255) & ~static_cast<size_t>(255);
+}
+
+}  // namespace
+}  // namespace seqattn
+
+using namespace seqattn;
+
+extern "C" {
+
+seqattn_status seqattn_chunk_fwd(const seqattn_problem* pb, int64_t q_start, int64_t q_len,
+                                 int64_t prefix_len, float softmax_scale, const void* q,
+                                 const void* k, const void* v, void* o, float* lse,
+                                 seqattn_stream_t stream) {
+  ChunkGeom g;
+  seqattn_status s = check_chunk(pb, q_start, q_len, prefix_len, softmax_scale, &g);
+  if (s != SEQATTN_OK) return s;
+  if (q_len == 0) return ok();
+  s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}});
+  if (s != SEQATTN_OK) return s;
+  unsigned int* err = nullptr;
+  cudaError_t e = error_word(&err);
+  if (e != cudaSuccess) return cuda_fail(e, "error word");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (pb->dtype == SEQATTN_FP32) {
+    e = launch_fwd_f32(g, static_cast<const float*>(q), static_cast<const float*>(k),
+                       static_cast<const float*>(v), static_cast<float*>(o), lse, err, st);
+    return e == cudaSuccess ? ok() : cuda_fail(e, "fwd_f32 launch");
+  }
+  Bf16FwdMaps maps;
+  if (!make_map(&maps.q, q, g.d, g.Hq, static_cast<int64_t>(g.B) * q_len, 128) ||
+      !make_map(&maps.k, k, g.d, g.Hkv, static_cast<int64_t>(g.B) * g.T, 128) ||
+      !make_map(&maps.v, v, g.d, g.Hkv, static_cast<int64_t>(g.B) * g.T, 128))
+    return fail(SEQATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the forward operands");
+  e = launch_fwd_bf16(g, maps, o, lse, err, st);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "fwd_bf16 launch");
+}
+
+seqattn_status seqattn_chunk_bwd(const seqattn_problem* pb, int64_t q_start, int64_t q_len,
+                                 int64_t prefix_len, float softmax_scale, const void* q,
+                                 const void* k, const void* v, const void* o, const float* lse,
+                                 const void* d_o, float* dq, float* dk_accum, float* dv_accum,
+                                 void* workspace, size_t workspace_size, seqattn_stream_t stream) {
+  ChunkGeom g;
+  seqattn_status s = check_chunk(pb, q_start, q_len, prefix_len, softmax_scale, &g);
+  if (s != SEQATTN_OK) return s;
+  if (q_len == 0) return ok();
+  s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}, {d_o, "d_o"}, {dq, "dq"},
+                  {dk_accum, "dk_accum"}, {dv_accum, "dv_accum"}, {workspace, "workspace"}});
+  if (s != SEQATTN_OK) return s;
+  if (workspace_size < workspace_bytes(pb, q_len))
+    return fail(SEQATTN_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace_size, workspace_bytes(pb, q_len));
+  unsigned int* err = nullptr;
+  cudaError_t e = error_word(&err);
+  if (e != cudaSuccess) return cuda_fail(e, "error word");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  float* delta = static_cast<float*>(workspace);
+  if (pb->dtype == SEQATTN_FP32) {
+    e = launch_bwd_prep_f32(g, static_cast<const float*>(o), static_cast<const float*>(d_o), delta,
+                            st);
+    if (e != cudaSuccess) return cuda_fail(e, "bwd_prep launch");
+    e = launch_bwd_f32(g, static_cast<const float*>(q), static_cast<const float*>(k),
+                       static_cast<const float*>(v), lse, static_cast<const float*>(d_o), delta,
+                       dq, dk_accum, dv_accum, err, st);
+    return e == cudaSuccess ? ok() : cuda_fail(e, "bwd_f32 launch");
+  }
+  Bf16BwdMaps maps;
+  if (!make_map(&maps.q, q, g.d, g.Hq, static_cast<int64_t>(g.B) * q_len, 64) ||
+      !make_map(&maps.d_o, d_o, g.d, g.Hq, static_cast<int64_t>(g.B) * q_len, 64) ||
+      !make_map(&maps.k, k, g.d, g.Hkv, static_cast<int64_t>(g.B) * g.T, 128) ||
+      !make_map(&maps.v, v, g.d, g.Hkv, static_cast<int64_t>(g.B) * g.T, 128))
+    return fail(SEQATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the backward operands");
+  e = launch_bwd_prep_bf16(g, o, d_o, delta, dq, st);
+  if (e != cudaSuccess) return cuda_fail(e, "bwd_prep launch");
+  e = launch_bwd_bf16(g, maps, lse, delta, dq, dk_accum, dv_accum, err, st);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "bwd_bf16 launch");
+}
+
+seqattn_status seqattn_reset_accum(const seqattn_problem* pb, float* dk_accum, float* dv_accum,
+                                   seqattn_stream_t stream) {
+  seqattn_status s = check_problem(pb);
+  if (s != SEQATTN_OK) return s;
+  s = check_ptrs({{dk_accum, "dk_accum"}, {dv_accum, "dv_accum"}});
+  if (s != SEQATTN_OK) return s;
+  const int64_t n = static_cast<int64_t>(pb->batch) * pb->seq_capacity * pb->num_kv_heads *
+                    pb->head_dim;
+  cudaError_t e = launch_zero_f32(dk_accum, dv_accum, n, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "reset launch");
+}
+
+size_t seqattn_bwd_workspace_size(const seqattn_problem* pb, int64_t q_len) {
+  if (check_problem(pb) != SEQATTN_OK || q_len < 0) return 0;
+  return workspace_bytes(pb, q_len);
+}
+
+seqattn_status seqattn_sync_status(seqattn_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  unsigned int* err = nullptr;
+  if ((e = error_word(&err)) != cudaSuccess) return cuda_fail(e, "error word");
+  unsigned int w = 0;
+  if ((e = cudaMemcpy(&w, err, sizeof(w), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "read error word");
+  if (w != 0) {
+    const unsigned int zero = 0;
+    if ((e = cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e, "clear error word");
+    return fail(SEQATTN_ERR_TIMEOUT, "a kernel gave up a bounded wait (error word 0x%x)", w);
+  }
+  return ok();
+}
+
+const char* seqattn_status_string(seqattn_status s) {
+  switch (s) {
+    case SEQATTN_OK: return "ok";
+    case SEQATTN_ERR_INVALID_ARG: return "invalid argument";
+    case SEQATTN_ERR_UNSUPPORTED: return "unsupported";
+    case SEQATTN_ERR_CUDA: return "CUDA error";
+    case SEQATTN_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* seqattn_last_error(void) { return t_last_error.c_str(); }
+
+}  // extern "C"

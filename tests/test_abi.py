@@ -1,0 +1,112 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and
+loads, exports every entry point include/seqattn.h declares, and rejects bad
+arguments with a status code before anything is launched."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from long_context_attention_seqattn_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load_library()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "seqattn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(seqattn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_surface():
+    assert _declared() == sorted(binding.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert lib.seqattn_status_string(0) == b"ok"
+    assert lib.seqattn_status_string(4) == b"device wait timed out"
+    assert lib.seqattn_status_string(99) == b"unknown status"
+
+
+def _pb(**kw):
+    base = dict(batch=1, num_q_heads=4, num_kv_heads=2, head_dim=128, seq_capacity=1024, dtype=0)
+    base.update(kw)
+    return binding.Problem(**base)
+
+
+def test_workspace_size(lib):
+    pb = _pb()
+    assert lib.seqattn_bwd_workspace_size(ctypes.byref(pb), 512) == 4 * 512 * 4
+    assert lib.seqattn_bwd_workspace_size(ctypes.byref(pb), 1) == 256
+    assert lib.seqattn_bwd_workspace_size(ctypes.byref(_pb(num_q_heads=3)), 512) == 0
+    assert lib.seqattn_bwd_workspace_size(None, 512) == 0
+
+
+P = ctypes.c_void_p(0x10000)      # aligned fake device address: never dereferenced here
+MIS = ctypes.c_void_p(0x10004)    # misaligned
+NUL = ctypes.c_void_p(0)
+
+
+def _fwd(lib, pb, q_start=0, q_len=128, prefix=0, scale=0.088, ptrs=None):
+    ptrs = ptrs or [P] * 5
+    st = lib.seqattn_chunk_fwd(ctypes.byref(pb) if pb is not None else None, q_start, q_len, prefix,
+                               scale, *ptrs, NUL)
+    return st, lib.seqattn_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_q_heads=3), 1),            # Hq % Hkv != 0
+    (dict(head_dim=96), 1),              # unsupported head_dim
+    (dict(batch=0), 1),
+    (dict(dtype=7), 1),
+    (dict(head_dim=64), 2),              # bf16 path needs d=128
+])
+def test_problem_validation(lib, kw, code):
+    st, msg = _fwd(lib, _pb(**kw))
+    assert st == code and msg
+
+
+def test_chunk_validation(lib):
+    pb = _pb()
+    assert _fwd(lib, None)[0] == 1
+    assert _fwd(lib, pb, q_len=-1)[0] == 1
+    assert _fwd(lib, pb, q_start=128, prefix=256)[0] == 1          # prefix beyond start
+    assert _fwd(lib, pb, q_start=1024, q_len=128, prefix=0)[0] == 1  # past the cache
+    assert _fwd(lib, pb, scale=0.0)[0] == 1
+    assert _fwd(lib, pb, scale=float("nan"))[0] == 1
+    assert _fwd(lib, pb, q_start=64, q_len=128, prefix=64)[0] == 2   # ragged bf16
+    assert _fwd(lib, pb, ptrs=[P, NUL, P, P, P])[0] == 1
+    st, msg = _fwd(lib, pb, ptrs=[P, P, P, MIS, P])
+    assert st == 1 and "aligned" in msg
+
+
+def test_empty_chunk_is_ok_without_touching_memory(lib):
+    assert _fwd(lib, _pb(), q_len=0, ptrs=[NUL] * 5)[0] == 0
+    st = lib.seqattn_chunk_bwd(ctypes.byref(_pb()), 0, 0, 0, 0.1, *([NUL] * 10), 0, NUL)
+    assert st == 0
+
+
+def test_bwd_validation(lib):
+    pb = _pb()
+    args = [P] * 10
+    st = lib.seqattn_chunk_bwd(ctypes.byref(pb), 0, 128, 0, 0.1, *args, 16, NUL)
+    assert st == 1 and b"workspace" in lib.seqattn_last_error()
+    args[9] = NUL
+    assert lib.seqattn_chunk_bwd(ctypes.byref(pb), 0, 128, 0, 0.1, *args, 1 << 20, NUL) == 1
+
+
+def test_reset_validation(lib):
+    assert lib.seqattn_reset_accum(ctypes.byref(_pb()), NUL, P, NUL) == 1
+    assert lib.seqattn_reset_accum(None, P, P, NUL) == 1

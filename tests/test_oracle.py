@@ -253,7 +253,8 @@ def test_row_and_tail_helpers_match_the_layer():
         assert abs(lrow - lse[0, h, r]) < 1e-13
         dqr = oracle.row_dq(q[0, r, h], do[0, r, h], o[0, r, h], k[0, :, g], v[0, :, g], r, 0, scale)
         np.testing.assert_allclose(dqr, dq[0, r, h], atol=1e-13)
-    t = oracle.tail_block(q, k, v, do, 29, 0, 1, scale, row_block=4)
+    t = oracle.tail_block(q[0, 29:, 2:4], k[0, :, 1], v[0, :, 1], do[0, 29:, 2:4], 29, scale,
+                          row_block=4)
     np.testing.assert_allclose(t["o"], o[0, 29:, 2:4], atol=1e-13)
     np.testing.assert_allclose(t["lse"], lse[0, 2:4, 29:], atol=1e-13)
     np.testing.assert_allclose(t["dq"], dq[0, 29:, 2:4], atol=1e-13)

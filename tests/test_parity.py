@@ -1,0 +1,269 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle on
+the same seeded inputs.
+
+Bars: float32 -> rel-L2 <= 1e-5 per output tensor; bf16 -> rel-L2 <= 2e-2 and
+max-abs <= 5e-2 per output tensor; D-chunk against D=1 within the bf16 bar.
+rel-L2 = ||x - y||_2 / ||y||_2 over the whole tensor, y the reference."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from long_context_attention_seqattn_gb300 import binding, inputs, workloads
+
+pytestmark = pytest.mark.gpu
+
+F32_REL = 1e-5
+BF16_REL = 2e-2
+BF16_ABS = 5e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from long_context_attention_seqattn_gb300 import build
+    build.build()
+    binding.load_library()
+    yield
+    binding.sync_status()
+
+
+def rel_l2(x, y):
+    x = np.asarray(x, dtype=np.float64)
+    y = np.asarray(y, dtype=np.float64)
+    return float(np.linalg.norm(x - y) / max(np.linalg.norm(y), 1e-300))
+
+
+def max_abs(x, y):
+    return float(np.abs(np.asarray(x, dtype=np.float64) - np.asarray(y, dtype=np.float64)).max())
+
+
+def assert_bf16(name, got, ref):
+    r, a = rel_l2(got, ref), max_abs(got, ref)
+    assert r <= BF16_REL and a <= BF16_ABS, f"{name}: rel-L2 {r:.3e} max-abs {a:.3e}"
+
+
+def assert_f32(name, got, ref):
+    r = rel_l2(got, ref)
+    assert r <= F32_REL, f"{name}: rel-L2 {r:.3e}"
+
+
+def cpu64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def run_layer(q, k, v, do, chunk, order="descending"):
+    bufs = binding.layer_forward_backward(q, k, v, do, chunk, bwd_order=order)
+    binding.sync_status()
+    return bufs
+
+
+def small_inputs(B, T, Hq, Hkv, d, dtype, seed):
+    dt = inputs.torch_dtype(dtype)
+    return [inputs.draw(n, seed, B, T, h, d, dt) for n, h in (("q", Hq), ("k", Hkv), ("v", Hkv), ("do", Hq))]
+
+
+# ============================================================== float32 path
+
+def _check_f32_layer(B, T, Hq, Hkv, d, chunk, seed, order="descending"):
+    cpu = small_inputs(B, T, Hq, Hkv, d, "fp32", seed)
+    q, k, v, do = (x.cuda() for x in cpu)
+    bufs = run_layer(q, k, v, do, chunk, order)
+    o, lse, dq, dk, dv = oracle.chunked_layer(*(x.numpy() for x in cpu), chunk, d ** -0.5)
+    assert_f32("O", cpu64(bufs.o), o)
+    assert_f32("LSE", cpu64(binding.gather_lse(bufs)), lse)
+    assert_f32("dQ", cpu64(bufs.dq), dq)
+    assert_f32("dK", cpu64(bufs.dk), dk)
+    assert_f32("dV", cpu64(bufs.dv), dv)
+
+
+def test_fp32_tiny_exactness_workload():
+    w = workloads.WORKLOADS["tiny-fp32-t512-c128"]
+    _check_f32_layer(w.batch, w.seq, w.hq, w.hkv, w.head_dim, w.chunk, w.seed)
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,d,chunk", [
+    (2, 300, 4, 2, 128, 100),    # ragged chunks, GQA, d=128, batch 2
+    (1, 257, 8, 1, 64, 64),      # ragged tail of one row, G=8
+    (1, 96, 3, 3, 64, 96),       # single chunk (D=1), MHA
+])
+def test_fp32_ragged_shapes(B, T, Hq, Hkv, d, chunk):
+    _check_f32_layer(B, T, Hq, Hkv, d, chunk, seed=11)
+
+
+def test_fp32_ascending_order_matches():
+    _check_f32_layer(1, 256, 2, 1, 64, 64, seed=5, order="ascending")
+
+
+def test_fp32_truncated_prefix_single_chunk():
+    B, T, Hq, Hkv, d = 1, 200, 2, 1, 64
+    cpu = small_inputs(B, T, Hq, Hkv, d, "fp32", 21)
+    q, k, v, do = (x.cuda() for x in cpu)
+    qs, c, p = 120, 50, 37
+    o = torch.empty((B, c, Hq, d), device="cuda")
+    lse = torch.empty((B, Hq, c), device="cuda")
+    binding.chunk_fwd(q[:, qs:qs + c].contiguous(), k, v, o, lse, qs, p)
+    dq = torch.empty((B, c, Hq, d), device="cuda")
+    dk = torch.zeros_like(k)
+    dv = torch.zeros_like(v)
+    binding.chunk_bwd(q[:, qs:qs + c].contiguous(), k, v, o, lse, do[:, qs:qs + c].contiguous(),
+                      dq, dk, dv, qs, p)
+    binding.sync_status()
+    qn, kn, vn, don = (x.numpy() for x in cpu)
+    ro, rl = oracle.chunk_forward(qn[:, qs:qs + c], kn, vn, qs, p, d ** -0.5)
+    rdk, rdv = np.zeros(kn.shape), np.zeros(vn.shape)
+    rdq = oracle.chunk_backward(qn[:, qs:qs + c], kn, vn, ro, rl, don[:, qs:qs + c], qs, p,
+                                d ** -0.5, rdk, rdv)
+    assert_f32("O", cpu64(o), ro)
+    assert_f32("LSE", cpu64(lse), rl)
+    assert_f32("dQ", cpu64(dq), rdq)
+    assert_f32("dK", cpu64(dk), rdk)
+    assert_f32("dV", cpu64(dv), rdv)
+    # rows outside [q_start - prefix_len, q_start + c) untouched
+    assert float(dk[:, :qs - p].abs().max()) == 0.0 and float(dk[:, qs + c:].abs().max()) == 0.0
+
+
+def test_fp32_guard_bands_untouched():
+    """Outputs embedded in larger buffers filled with a canary: the kernels
+    write only inside their tensors."""
+    B, T, Hq, Hkv, d, c = 1, 256, 2, 2, 64, 128
+    cpu = small_inputs(B, T, Hq, Hkv, d, "fp32", 3)
+    q, k, v, do = (x.cuda() for x in cpu)
+    canary = 12345.0
+    pad = 4096
+    big_o = torch.full((pad * 2 + B * c * Hq * d,), canary, device="cuda")
+    big_l = torch.full((pad * 2 + B * Hq * c,), canary, device="cuda")
+    o = big_o[pad:pad + B * c * Hq * d].view(B, c, Hq, d)
+    lse = big_l[pad:pad + B * Hq * c].view(B, Hq, c)
+    binding.chunk_fwd(q[:, 128:].contiguous(), k, v, o, lse, 128)
+    binding.sync_status()
+    for big in (big_o, big_l):
+        assert float((big[:pad] != canary).sum()) == 0 and float((big[-pad:] != canary).sum()) == 0
+
+
+def test_empty_chunk_no_op():
+    k = torch.zeros((1, 256, 2, 128), dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros((1, 0, 4, 128), dtype=torch.bfloat16, device="cuda")
+    o = torch.zeros_like(q)
+    lse = torch.zeros((1, 4, 0), device="cuda")
+    binding.chunk_fwd(q, k, k, o, lse, 128)
+    binding.sync_status()
+
+
+# ============================================================== bf16 tensor-core path
+
+def _bf16_group_check(w, cpu, bufs, chunk, groups):
+    """Full comparison for the given key/value groups (all their query heads),
+    against the oracle run on just those heads (groups are independent)."""
+    q, k, v, do = cpu
+    G = w.hq // w.hkv
+    for g in groups:
+        hs = slice(g * G, (g + 1) * G)
+        args = [x.to(torch.float64).numpy() for x in (q[:, :, hs], k[:, :, g:g + 1], v[:, :, g:g + 1],
+                                                       do[:, :, hs])]
+        o, lse, dq, dk, dv = oracle.chunked_layer(*args, chunk, w.scale)
+        assert_bf16(f"O g{g}", cpu64(bufs.o[:, :, hs]), o)
+        assert_bf16(f"LSE g{g}", cpu64(binding.gather_lse(bufs)[:, hs]), lse)
+        assert_bf16(f"dQ g{g}", cpu64(bufs.dq[:, :, hs]), dq)
+        assert_bf16(f"dK g{g}", cpu64(bufs.dk[:, :, g:g + 1]), dk)
+        assert_bf16(f"dV g{g}", cpu64(bufs.dv[:, :, g:g + 1]), dv)
+
+
+def test_bf16_small_multi_tile():
+    """Several q tiles and key tiles, GQA, two chunks plus the D=1 pass."""
+    B, T, Hq, Hkv, d = 1, 768, 4, 2, 128
+    w = workloads.Workload("small", B, T, Hq, Hkv, d, "bf16", (256,), 40)
+    cpu = small_inputs(B, T, Hq, Hkv, d, "bf16", 40)
+    dev = [x.cuda() for x in cpu]
+    for chunk in (256, 384, 768):
+        bufs = run_layer(*dev, chunk)
+        _bf16_group_check(w, cpu, bufs, chunk, range(Hkv))
+
+
+def test_bf16_qwen3_4b_layer_two_groups():
+    w = workloads.WORKLOADS["qwen3-4b-layer-t8192-c512"]
+    cpu = inputs.layer_inputs(w)
+    dev = [x.cuda() for x in cpu]
+    bufs = run_layer(*dev, w.chunk)
+    _bf16_group_check(w, cpu, bufs, w.chunk, (0, w.hkv - 1))
+
+
+def _sampled_check(w, bufs, groups, n_tail=256, sample_rows=(0, 1, 127, 128, 2047, 2048)):
+    """Sampled rows of a full-size layer against the oracle, computed one by
+    one from regenerated inputs (never from the GPU): the last n_tail rows and
+    keys of the given groups in full (dK/dV of tail keys only involve tail
+    rows), plus O/LSE/dQ of chosen rows anywhere in the sequence."""
+    G = w.hq // w.hkv
+    dt = inputs.torch_dtype(w.dtype)
+    T, d = w.seq, w.head_dim
+    lse_all = binding.gather_lse(bufs)
+    for g in groups:
+        k = inputs.draw_rows("k", w.seed, 0, 0, T, w.hkv, d, dt)[:, g].to(torch.float64).numpy()
+        v = inputs.draw_rows("v", w.seed, 0, 0, T, w.hkv, d, dt)[:, g].to(torch.float64).numpy()
+        j0 = T - n_tail
+        qt = inputs.draw_rows("q", w.seed, 0, j0, T, w.hq, d, dt)[:, g * G:(g + 1) * G]
+        dot = inputs.draw_rows("do", w.seed, 0, j0, T, w.hq, d, dt)[:, g * G:(g + 1) * G]
+        ref = oracle.tail_block(qt.to(torch.float64).numpy(), k, v, dot.to(torch.float64).numpy(),
+                                j0, w.scale)
+        hs = slice(g * G, (g + 1) * G)
+        assert_bf16(f"tail O g{g}", cpu64(bufs.o[0, j0:, hs]), ref["o"])
+        assert_bf16(f"tail LSE g{g}", cpu64(lse_all[0, hs, j0:]), ref["lse"])
+        assert_bf16(f"tail dQ g{g}", cpu64(bufs.dq[0, j0:, hs]), ref["dq"])
+        assert_bf16(f"tail dK g{g}", cpu64(bufs.dk[0, j0:, g]), ref["dk"])
+        assert_bf16(f"tail dV g{g}", cpu64(bufs.dv[0, j0:, g]), ref["dv"])
+        got_o, ref_o, got_dq, ref_dq, got_l, ref_l = [], [], [], [], [], []
+        for r in sample_rows:
+            qr = inputs.draw_rows("q", w.seed, 0, r, r + 1, w.hq, d, dt)[0].to(torch.float64).numpy()
+            dr = inputs.draw_rows("do", w.seed, 0, r, r + 1, w.hq, d, dt)[0].to(torch.float64).numpy()
+            for h in (g * G, g * G + G - 1):
+                o_r, l_r = oracle.row_forward(qr[h], k, v, r, 0, w.scale)
+                ref_o.append(o_r)
+                ref_l.append(l_r)
+                ref_dq.append(oracle.row_dq(qr[h], dr[h], o_r, k, v, r, 0, w.scale))
+                got_o.append(cpu64(bufs.o[0, r, h]))
+                got_l.append(float(lse_all[0, h, r]))
+                got_dq.append(cpu64(bufs.dq[0, r, h]))
+        assert_bf16(f"rows O g{g}", np.array(got_o), np.array(ref_o))
+        assert_bf16(f"rows LSE g{g}", np.array(got_l), np.array(ref_l))
+        assert_bf16(f"rows dQ g{g}", np.array(got_dq), np.array(ref_dq))
+
+
+def _sum_invariant(w, bufs):
+    """sum_j dV[j] = sum over the group's rows of dO, at any size."""
+    G = w.hq // w.hkv
+    do = inputs.draw("do", w.seed, w.batch, w.seq, w.hq, w.head_dim, inputs.torch_dtype(w.dtype))
+    ref = do.to(torch.float64).view(w.batch, w.seq, w.hkv, G, w.head_dim).sum((1, 3))
+    got = bufs.dv.to(torch.float64).sum(1).cpu()
+    assert_bf16("sum_j dV", got.numpy(), ref.numpy())
+
+
+def test_bf16_llama3_8b_layer_sampled():
+    w = workloads.WORKLOADS["llama3-8b-layer-t32768-c2048"]
+    dev = inputs.layer_inputs(w, device="cuda")
+    bufs = run_layer(*dev, w.chunk)
+    _sampled_check(w, bufs, (0, w.hkv - 1), sample_rows=(0, 1, 2047, 2048, 16383, 30720, 32767))
+    _sum_invariant(w, bufs)
+
+
+def test_bf16_32b_layer_t131072_sampled():
+    w = workloads.WORKLOADS["32b-layer-t131072-c4096"]
+    dev = inputs.layer_inputs(w, device="cuda")
+    bufs = run_layer(*dev, w.chunk)
+    _sampled_check(w, bufs, (0,), sample_rows=(0, 4095, 4096, 65536, 131071))
+
+
+def test_bf16_partition_sweep_agrees_with_unchunked():
+    w = workloads.WORKLOADS["partition-sweep-t16384"]
+    cpu = inputs.layer_inputs(w)
+    dev = [x.cuda() for x in cpu]
+    ref = run_layer(*dev, 16384)
+    ref_t = [x.clone() for x in (ref.o, binding.gather_lse(ref), ref.dq, ref.dk, ref.dv)]
+    # D=1 against the oracle on one key/value group
+    _bf16_group_check(w, cpu, ref, 16384, (w.hkv - 1,))
+    for chunk in w.chunks[:-1]:
+        bufs = run_layer(*dev, chunk)
+        got = (bufs.o, binding.gather_lse(bufs), bufs.dq, bufs.dk, bufs.dv)
+        for name, a, b in zip(("O", "LSE", "dQ", "dK", "dV"), got, ref_t):
+            assert_bf16(f"c={chunk} {name} vs D=1", cpu64(a), cpu64(b))
