@@ -255,32 +255,31 @@ def row_dq(q_row, do_row, o_row, k_head, v_head, row_pos, kv_begin, scale):
     return scale * (ds @ K)
 
 
-def tail_block(q, k, v, do, j0, b, g, scale, row_block=64):
-    """Whole-layer outputs restricted to the sequence tail [j0, T) for batch b
-    and key/value head g (all G query heads of that group), straight from the
+def tail_block(q_tail, k_head, v_head, do_tail, j0, scale, row_block=64):
+    """Whole-layer outputs restricted to the sequence tail [j0, T) for ONE
+    key/value head and the G query heads of its group, straight from the
     full-sequence definition.  Because of causality, dK[j] and dV[j] for
     j >= j0 receive contributions only from query rows r >= j >= j0, so this
-    tail is exact without touching rows before j0 (StreamBP review page,
+    tail is exact without touching query rows before j0 (StreamBP review page,
     Property 3.1).
 
-    q, do: [B, T, Hq, d]; k, v: [B, T, Hkv, d].  Returns a dict with
-    o [T-j0, G, d], lse [G, T-j0], dq [T-j0, G, d], dk [T-j0, d], dv [T-j0, d]
-    (query heads in group order h = g*G .. g*G+G-1)."""
-    B, T, Hq, d = q.shape
-    Hkv = k.shape[2]
-    G = Hq // Hkv
-    n = T - j0
-    K = _as64(k[b, :, g, :])
-    V = _as64(v[b, :, g, :])
+    q_tail, do_tail: [T-j0, G, d] (rows j0..T-1 of the group's query heads);
+    k_head, v_head: [T, d] (the whole cache of that key/value head).
+    Returns a dict with o [T-j0, G, d], lse [G, T-j0], dq [T-j0, G, d],
+    dk [T-j0, d], dv [T-j0, d]."""
+    K = _as64(k_head)
+    V = _as64(v_head)
+    T, d = K.shape
+    n, G, _ = q_tail.shape
+    assert n == T - j0
     out = {"o": np.zeros((n, G, d)), "lse": np.zeros((G, n)), "dq": np.zeros((n, G, d)),
            "dk": np.zeros((n, d)), "dv": np.zeros((n, d))}
     for gi in range(G):
-        h = g * G + gi
         for r0 in range(j0, T, row_block):
             r1 = min(r0 + row_block, T)
             rows = np.arange(r0, r1)
-            Qr = _as64(q[b, r0:r1, h, :])
-            dOr = _as64(do[b, r0:r1, h, :])
+            Qr = _as64(q_tail[r0 - j0:r1 - j0, gi])
+            dOr = _as64(do_tail[r0 - j0:r1 - j0, gi])
             S = scale * (Qr @ K[:r1].T)                      # keys [0, r1)
             vis = np.arange(r1)[None, :] <= rows[:, None]
             S = np.where(vis, S, -np.inf)
