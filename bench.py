@@ -1,0 +1,356 @@
+#!/usr/bin/env python
+"""Benchmark of the chunked causal-attention layer pass (StreamBP / SeCO chunk
+calls): reset the dK/dV running sums, forward every chunk, backward every chunk
+last to first, all through the libseqattn C ABI.
+
+Metric: causal fwd+bwd TFLOP/s (14 * B * Hq * d * T(T+1)/2 FLOPs credited per
+pass).  One JSON line on stdout (rank 0).  Usage:
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+With N > 1 it is launched by torchrun, one process per GPU; every rank runs
+its own independent problems (weak scaling, no data-path collective) and the
+timing is the max over ranks.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "chunked causal attn fwd+bwd TFLOP/s (causal FLOPs) and % of GB300 BF16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_SUSTAINED_TFLOPS = 1700.0   # used only when no measured peaks file exists
+
+# DRAM traffic (bytes read + written) per backward launch, from the ncu
+# capture summarised under profiles/; None until measured for this kernel.
+BWD_TRAFFIC_BYTES_PER_LAUNCH = None
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            pk = json.load(fh)
+        return float(pk["bf16_tflops_sustained"]), "measured (sustained cuBLAS bf16, MEASURED_PEAKS.json)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_SUSTAINED_TFLOPS, "fallback (sustained bf16)"
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+
+def oracle_sample(w, seed, heads):
+    """Bounded sample of the workload for the float64 oracle: the last chunk
+    (the longest prefix), forward + backward, for `heads` query heads of key/value
+    head 0.  Returns (credited causal FLOPs, seconds, description)."""
+    import oracle
+    import torch
+    from long_context_attention_seqattn_gb300 import inputs, workloads
+
+    dt = inputs.torch_dtype(w.dtype)
+    s = workloads.chunk_starts(w.seq, w.chunk)[-1]
+    c = min(w.chunk, w.seq - s)
+    d = w.head_dim
+
+    def rows(name, r0, r1, H, hs):
+        return inputs.draw_rows(name, seed, 0, r0, r1, H, d, dt)[:, hs].to(torch.float64).numpy()[None]
+
+    q = rows("q", s, s + c, w.hq, slice(0, heads))
+    do = rows("do", s, s + c, w.hq, slice(0, heads))
+    k = rows("k", 0, s + c, w.hkv, slice(0, 1))
+    v = rows("v", 0, s + c, w.hkv, slice(0, 1))
+    import numpy as np
+    t0 = time.perf_counter()
+    o, lse = oracle.chunk_forward(q, k, v, s, s, w.scale)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    oracle.chunk_backward(q, k, v, o, lse, do, s, s, w.scale, dk, dv)
+    secs = time.perf_counter() - t0
+    flops = 14 * heads * d * workloads.causal_pairs(s, c)
+    desc = (f"float64 NumPy oracle, last chunk (rows {s}..{s + c - 1}, prefix {s}) fwd+bwd for "
+            f"{heads} query head(s) of key/value head 0; credited causal FLOPs {flops:.3e}")
+    return flops, secs, desc
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, w):
+    from long_context_attention_seqattn_gb300 import dist
+    rank, world = dist.init("gloo")
+    if rank != 0:
+        dist.finalize()
+        return
+    for _ in range(args.warmup):
+        oracle_sample(w, w.seed, 1)
+    flops = secs = 0.0
+    desc = ""
+    for _ in range(args.steps):
+        f, s, desc = oracle_sample(w, w.seed, 1)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    dist.finalize()
+
+
+def workload_config(w):
+    in_bytes = 2 * (2 * w.batch * w.seq * w.hq * w.head_dim + 2 * w.batch * w.seq * w.hkv * w.head_dim)
+    return {"workload": w.name, "batch": w.batch, "seq_len": w.seq, "chunk": w.chunk,
+            "num_chunks": (w.seq + w.chunk - 1) // w.chunk, "num_q_heads": w.hq,
+            "num_kv_heads": w.hkv, "head_dim": w.head_dim,
+            "l2": f"inputs larger than L2: Q, K, V, dO = {in_bytes / 2**20:.0f} MiB per step"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, w):
+    import torch
+
+    from long_context_attention_seqattn_gb300 import binding, build, dist, inputs, workloads
+
+    rank, world = dist.init("nccl")
+    _, local_rank, _ = dist.rank_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    build.build()
+    binding.load_library()
+
+    # every rank owns its own batch entry of independent problems (weak scaling)
+    seed = w.seed + rank
+    q, k, v, do = inputs.layer_inputs(w, device=dev, seed=seed)
+    bufs = binding.LayerBuffers(q, k, w.chunk)
+    starts = bufs.starts
+    D = len(starts)
+    T, c = w.seq, w.chunk
+
+    def step(events=None):
+        binding.reset_accum(bufs.dk, bufs.dv, w.hq)
+        for i, s in enumerate(starts):
+            e = min(s + c, T)
+            if events is not None:
+                events["fwd"][i][0].record()
+            binding.chunk_fwd(q[:, s:e], k, v, bufs.o[:, s:e], bufs.lse_chunks[i], s)
+            if events is not None:
+                events["fwd"][i][1].record()
+        for i in range(D - 1, -1, -1):
+            s = starts[i]
+            e = min(s + c, T)
+            if events is not None:
+                events["bwd"][i][0].record()
+            binding.chunk_bwd(q[:, s:e], k, v, bufs.o[:, s:e], bufs.lse_chunks[i], do[:, s:e],
+                              bufs.dq[:, s:e], bufs.dk, bufs.dv, s, workspace=bufs.workspace)
+            if events is not None:
+                events["bwd"][i][1].record()
+
+    if (T % c) != 0 or w.batch != 1:
+        raise SystemExit("bench expects B=1 and T divisible by the chunk")
+
+    for _ in range(args.warmup):
+        step()
+    binding.sync_status()
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    launch_ev = [{"fwd": [(ev(), ev()) for _ in range(D)], "bwd": [(ev(), ev()) for _ in range(D)]}
+                 for _ in range(args.steps)]
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = None
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    time.sleep(0.3)
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = ev(), ev()
+    t0.record()
+    for kstep in range(args.steps):
+        step(launch_ev[kstep])
+    t1.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    clock_info = clocks.stop()
+    binding.sync_status()
+    ms_local = t0.elapsed_time(t1)
+    ms = dist.max_over_ranks(ms_local, device=dev)
+    flops_rank = w.causal_flops()
+    value = world * flops_rank * args.steps / (ms / 1e3) / 1e12
+
+    # per-launch roofline (live CUDA-event durations inside the timed region)
+    fwd_ms = sum(a.elapsed_time(b) for e in launch_ev for a, b in e["fwd"])
+    bwd_ms = sum(a.elapsed_time(b) for e in launch_ev for a, b in e["bwd"])
+    pairs = sum(workloads.causal_pairs(s, min(c, T - s)) for s in starts)
+    fwd_flops = 4 * w.batch * w.hq * w.head_dim * pairs * args.steps
+    bwd_flops = 10 * w.batch * w.hq * w.head_dim * pairs * args.steps
+    peak, peak_src = measured_peak()
+    bwd_tf = bwd_flops / (bwd_ms / 1e3) / 1e12
+    fwd_tf = fwd_flops / (fwd_ms / 1e3) / 1e12
+    roofline = {"kernel": "seqattn_chunk_bwd (Delta prep + bwd_bf16_kernel)", "bound": "tensor",
+                "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak,
+                "peak_source": peak_src,
+                "traffic": BWD_TRAFFIC_BYTES_PER_LAUNCH,
+                "per_launch": f"causal bwd FLOPs 10*Hq*d*pairs(chunk) averaged over {D} launches/step",
+                "avg_launch_ms": bwd_ms / (D * args.steps)}
+    roofline_fwd = {"kernel": "seqattn_chunk_fwd (fwd_bf16_kernel)", "bound": "tensor", "achieved": fwd_tf,
+                    "peak": peak, "unit": "TFLOP/s", "frac": fwd_tf / peak,
+                    "avg_launch_ms": fwd_ms / (D * args.steps)}
+
+    # end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_in = [x.to("cpu").pin_memory() for x in (q, k, v, do)]
+        outs = [bufs.o, *bufs.lse_chunks, bufs.dq, bufs.dk, bufs.dv]
+        h_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
+        h2d = sum(x.numel() * x.element_size() for x in h_in)
+        d2h = sum(x.numel() * x.element_size() for x in h_out)
+
+        def e2e_step():
+            for dst, src in zip((q, k, v, do), h_in):
+                dst.copy_(src, non_blocking=True)
+            binding.layer_forward_backward(q, k, v, do, c, bufs=bufs)
+            for dst, src in zip(h_out, outs):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        dist.barrier()
+        a, b = ev(), ev()
+        a.record()
+        for _ in range(args.steps):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        dist.barrier()
+        binding.sync_status()
+        e2e_ms = dist.max_over_ranks(a.elapsed_time(b), device=dev)
+        e2e = {"value": world * flops_rank * args.steps / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms / args.steps}
+
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        G = w.hq // w.hkv
+        f, s, desc = oracle_sample(w, w.seed, G)
+        cpu_baseline = {"value": f / s / 1e12, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                        "sample": desc, "seconds": s}
+
+    launches_per_step = 1 + D + 2 * D   # reset, fwd per chunk, (Delta prep + bwd) per chunk
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w),
+        "frac_of_peak": value / world / peak,
+        "roofline": roofline, "roofline_fwd": roofline_fwd,
+        "cpu_baseline": cpu_baseline, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clock_info,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.finalize()
+
+
+def main():
+    args = parse_args()
+    from long_context_attention_seqattn_gb300 import workloads
+    w = workloads.WORKLOADS[args.workload or workloads.BENCH_WORKLOAD]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()
