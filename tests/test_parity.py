@@ -231,12 +231,16 @@ def _sampled_check(w, bufs, groups, n_tail=256, sample_rows=(0, 1, 127, 128, 204
 
 
 def _sum_invariant(w, bufs):
-    """sum_j dV[j] = sum over the group's rows of dO, at any size."""
+    """sum_j dV[j] = sum over the group's rows of dO (softmax rows sum to one),
+    at any size.  The sums run over T*G terms of magnitude ~1, so the
+    element-wise absolute bar of the outputs does not apply to them: the check
+    is rel-L2 <= 2e-2 and max-abs <= 1e-3 of the largest |sum|."""
     G = w.hq // w.hkv
     do = inputs.draw("do", w.seed, w.batch, w.seq, w.hq, w.head_dim, inputs.torch_dtype(w.dtype))
-    ref = do.to(torch.float64).view(w.batch, w.seq, w.hkv, G, w.head_dim).sum((1, 3))
-    got = bufs.dv.to(torch.float64).sum(1).cpu()
-    assert_bf16("sum_j dV", got.numpy(), ref.numpy())
+    ref = do.to(torch.float64).view(w.batch, w.seq, w.hkv, G, w.head_dim).sum((1, 3)).numpy()
+    got = bufs.dv.to(torch.float64).sum(1).cpu().numpy()
+    r, a = rel_l2(got, ref), max_abs(got, ref)
+    assert r <= BF16_REL and a <= 1e-3 * np.abs(ref).max(), f"sum_j dV: rel-L2 {r:.3e} max-abs {a:.3e}"
 
 
 def test_bf16_llama3_8b_layer_sampled():
