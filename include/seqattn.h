@@ -32,7 +32,8 @@
  * Element type of q, k, v, o, d_o: bfloat16 for SEQATTN_BF16, float32 for
  * SEQATTN_FP32.  Every pointer is a DEVICE pointer owned by the caller and
  * must be 16-byte aligned; the library allocates nothing and keeps no state
- * between calls other than a device-side error word.
+ * between calls other than a device-side error word (and the fixed scratch
+ * array of seqattn_chunk_bwd_noalloc).
  *
  * All work is enqueued asynchronously on `stream` (a cudaStream_t; 0 is the
  * legacy default stream).  Argument errors are detected on the host before
@@ -113,6 +114,33 @@ seqattn_status seqattn_chunk_bwd(const seqattn_problem* pb, int64_t q_start, int
                                  const void* d_o, float* dq, float* dk_accum, float* dv_accum,
                                  void* workspace, size_t workspace_bytes,
                                  seqattn_stream_t stream);
+
+/*
+ * Backward of one chunk for callers that cannot allocate device memory.  The
+ * paper has no counterpart: this is a library convenience.  Some callers own
+ * no allocator of their own -- their device memory belongs to another
+ * allocator (a framework's caching allocator or a fixed arena) and the
+ * interface they call through passes only the tensors -- so they cannot
+ * provide the workspace seqattn_chunk_bwd asks for.  This entry point computes
+ * exactly what seqattn_chunk_bwd computes, with the same arguments minus the
+ * workspace, and calls no allocation routine.
+ *
+ * Its scratch (Delta, B * Hq * q_len floats) is a fixed device array inside
+ * the library of SEQATTN_NOALLOC_MAX_DELTA floats (4 MiB), which every GPU
+ * that loads the library holds until the process exits.  Larger requests
+ * return SEQATTN_ERR_INVALID_ARG (use seqattn_chunk_bwd instead).  The first
+ * call on a device looks up that device's address of the array; make that
+ * first call before any stream capture.  Every call shares the one array, so
+ * calls that overlap on the GPU (different streams, or different host
+ * threads) race on it and must be serialised by the caller.
+ */
+#define SEQATTN_NOALLOC_MAX_DELTA (1 << 20)
+seqattn_status seqattn_chunk_bwd_noalloc(const seqattn_problem* pb, int64_t q_start,
+                                         int64_t q_len, int64_t prefix_len, float softmax_scale,
+                                         const void* q, const void* k, const void* v,
+                                         const void* o, const float* lse, const void* d_o,
+                                         float* dq, float* dk_accum, float* dv_accum,
+                                         seqattn_stream_t stream);
 
 /* Zero both float32 accumulators ([B, T, Hkv, d] each) before the first chunk
  * of a backward pass (the running sum starts at zero). */

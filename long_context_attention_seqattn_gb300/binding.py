@@ -25,6 +25,7 @@ SEQATTN_FP32 = 1
 EXPORTED = (
     "seqattn_chunk_fwd",
     "seqattn_chunk_bwd",
+    "seqattn_chunk_bwd_noalloc",
     "seqattn_reset_accum",
     "seqattn_bwd_workspace_size",
     "seqattn_sync_status",
@@ -69,6 +70,9 @@ def load_library(path=LIB_PATH):
     lib.seqattn_chunk_bwd.argtypes = [P, i64, i64, i64, f32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                       vp, sz, vp]
     lib.seqattn_chunk_bwd.restype = ctypes.c_int
+    lib.seqattn_chunk_bwd_noalloc.argtypes = [P, i64, i64, i64, f32, vp, vp, vp, vp, vp, vp, vp,
+                                              vp, vp, vp]
+    lib.seqattn_chunk_bwd_noalloc.restype = ctypes.c_int
     lib.seqattn_reset_accum.argtypes = [P, vp, vp, vp]
     lib.seqattn_reset_accum.restype = ctypes.c_int
     lib.seqattn_bwd_workspace_size.argtypes = [P, i64]

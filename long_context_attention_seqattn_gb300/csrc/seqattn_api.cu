@@ -287,3 +287,89 @@ const char* seqattn_status_string(seqattn_status s) {
 const char* seqattn_last_error(void) { return t_last_error.c_str(); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward for callers that cannot allocate device memory.
+//
+// Some callers have no way to provide the backward's scratch buffer: their
+// device memory is owned by another allocator (a framework's caching
+// allocator or a fixed arena handed out at start-up) and the plugin interface
+// they call through passes only the tensors themselves.  For them the Delta
+// scratch lives in a fixed array in this file, so the call needs nothing
+// beyond its inputs and outputs.
+// ---------------------------------------------------------------------------
+namespace seqattn {
+namespace {
+
+// Delta scratch: B * Hq * q_len floats at most (4 MiB on every GPU that
+// loads the library, held until the process exits).
+static __device__ __align__(256) float g_noalloc_delta[SEQATTN_NOALLOC_MAX_DELTA];
+
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of this device's scratch array.  Host code cannot use the
+// array's name as a device pointer, so the address is looked up once per
+// device, with that device current, on the first call there.
+cudaError_t noalloc_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_delta);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace seqattn
+
+extern "C" seqattn_status seqattn_chunk_bwd_noalloc(
+    const seqattn_problem* pb, int64_t q_start, int64_t q_len, int64_t prefix_len,
+    float softmax_scale, const void* q, const void* k, const void* v, const void* o,
+    const float* lse, const void* d_o, float* dq, float* dk_accum, float* dv_accum,
+    seqattn_stream_t stream) {
+  ChunkGeom g;
+  seqattn_status s = check_chunk(pb, q_start, q_len, prefix_len, softmax_scale, &g);
+  if (s != SEQATTN_OK) return s;
+  if (q_len == 0) return ok();
+  s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}, {d_o, "d_o"}, {dq, "dq"},
+                  {dk_accum, "dk_accum"}, {dv_accum, "dv_accum"}});
+  if (s != SEQATTN_OK) return s;
+  const int64_t rows = static_cast<int64_t>(pb->batch) * pb->num_q_heads * q_len;
+  if (rows > SEQATTN_NOALLOC_MAX_DELTA)
+    return fail(SEQATTN_ERR_INVALID_ARG,
+                "batch * num_q_heads * q_len = %lld exceeds the fixed scratch of %d rows of "
+                "seqattn_chunk_bwd_noalloc; use seqattn_chunk_bwd with a workspace",
+                (long long)rows, SEQATTN_NOALLOC_MAX_DELTA);
+  float* delta = nullptr;
+  cudaError_t e = noalloc_scratch(&delta);
+  if (e != cudaSuccess) return cuda_fail(e, "scratch address");
+  unsigned int* err = nullptr;
+  if ((e = error_word(&err)) != cudaSuccess) return cuda_fail(e, "error word");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (pb->dtype == SEQATTN_FP32) {
+    e = launch_bwd_prep_f32(g, static_cast<const float*>(o), static_cast<const float*>(d_o), delta,
+                            st);
+    if (e != cudaSuccess) return cuda_fail(e, "bwd_prep launch");
+    e = launch_bwd_f32(g, static_cast<const float*>(q), static_cast<const float*>(k),
+                       static_cast<const float*>(v), lse, static_cast<const float*>(d_o), delta,
+                       dq, dk_accum, dv_accum, err, st);
+    return e == cudaSuccess ? ok() : cuda_fail(e, "bwd_f32 launch");
+  }
+  Bf16BwdMaps maps;
+  if (!make_map(&maps.q, q, g.d, g.Hq, static_cast<int64_t>(g.B) * q_len, 64) ||
+      !make_map(&maps.d_o, d_o, g.d, g.Hq, static_cast<int64_t>(g.B) * q_len, 64) ||
+      !make_map(&maps.k, k, g.d, g.Hkv, static_cast<int64_t>(g.B) * g.T, 128) ||
+      !make_map(&maps.v, v, g.d, g.Hkv, static_cast<int64_t>(g.B) * g.T, 128))
+    return fail(SEQATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the backward operands");
+  e = launch_bwd_prep_bf16(g, o, d_o, delta, dq, st);
+  if (e != cudaSuccess) return cuda_fail(e, "bwd_prep launch");
+  e = launch_bwd_bf16(g, maps, lse, delta, dq, dk_accum, dv_accum, err, st);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "bwd_bf16 launch");
+}
