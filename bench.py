@@ -31,8 +31,9 @@ UNIT = "TFLOP/s"
 FALLBACK_SUSTAINED_TFLOPS = 1700.0   # used only when no measured peaks file exists
 
 # DRAM traffic (bytes read + written) per backward launch, from the ncu
-# capture summarised under profiles/; None until measured for this kernel.
-BWD_TRAFFIC_BYTES_PER_LAUNCH = None
+# capture summarised under profiles/ (average over the 16 chunk launches of the
+# bench workload); set to None whenever the kernel changes until re-measured.
+BWD_TRAFFIC_BYTES_PER_LAUNCH = 401.3e6   # bwd_bf16_kernel, 3-stage ring (launches_llama3-8b-layer-t32768-c2048.md)
 
 
 def parse_args():
@@ -342,12 +343,61 @@ def run_ours(args, w):
     dist.finalize()
 
 
+def run_sweep(args, w):
+    """Partition-size sweep (one GPU): the same T=16384 layer at every chunk
+    size, each pass replayed from a CUDA graph so that small chunks measure
+    the kernels rather than host launch overhead.  Prints one JSON line whose
+    value is the smallest chunk's throughput, with the whole sweep and each
+    size's overhead against the unchunked pass."""
+    import torch
+
+    from long_context_attention_seqattn_gb300 import binding, build, inputs
+
+    torch.cuda.set_device(0)
+    build.build()
+    binding.load_library()
+    q, k, v, do = inputs.layer_inputs(w, device="cuda")
+    flops = w.causal_flops()
+    rows = []
+    for c in w.chunks:
+        graph = binding.LayerGraph(q, k, v, do, c)
+        for _ in range(args.warmup):
+            graph.replay()
+        binding.sync_status()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(args.steps):
+            graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        binding.sync_status()
+        ms = a.elapsed_time(b) / args.steps
+        rows.append({"chunk": c, "num_chunks": (w.seq + c - 1) // c, "ms_per_step": ms,
+                     "value": flops / (ms / 1e3) / 1e12, "gpu_launches_per_step": 1 + 3 * ((w.seq + c - 1) // c)})
+        del graph
+    base = next(r for r in rows if r["num_chunks"] == 1)
+    for r in rows:
+        r["time_vs_unchunked"] = r["ms_per_step"] / base["ms_per_step"]
+    first = rows[0]
+    peak, _ = measured_peak()
+    line = {"metric": METRIC, "value": first["value"], "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": first["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(workload_config(w), chunk=first["chunk"], num_chunks=first["num_chunks"]),
+            "frac_of_peak": first["value"] / peak, "sweep": rows,
+            "gpu_launches": first["gpu_launches_per_step"] * args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     from long_context_attention_seqattn_gb300 import workloads
     w = workloads.WORKLOADS[args.workload or workloads.BENCH_WORKLOAD]
     if args.impl == "reference":
         run_reference(args, w)
+    elif len(w.chunks) > 1:
+        run_sweep(args, w)
     else:
         run_ours(args, w)
 

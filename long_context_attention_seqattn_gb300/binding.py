@@ -253,3 +253,29 @@ def layer_forward_backward(q, k, v, d_o, chunk, scale=None, bufs=None, stream=No
 def gather_lse(bufs):
     """Concatenate the per-chunk LSE buffers into [B, Hq, T]."""
     return torch.cat(bufs.lse_chunks, dim=2)
+
+
+class LayerGraph:
+    """One layer pass (reset, D chunk forwards, D chunk backwards) captured
+    into a CUDA graph, so that small chunks are not bound by host launch
+    overhead.  ``replay()`` re-runs it on the same input and output buffers
+    (update the inputs in place between replays)."""
+
+    def __init__(self, q, k, v, d_o, chunk, scale=None, bufs=None, bwd_order="descending"):
+        self.args = (q, k, v, d_o, chunk)
+        self.bufs = bufs if bufs is not None else LayerBuffers(q, k, chunk)
+        # one eager pass first: loads the kernels and looks up the per-device
+        # error word outside the capture
+        layer_forward_backward(q, k, v, d_o, chunk, scale, self.bufs, bwd_order=bwd_order)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(self.graph, stream=side):
+                layer_forward_backward(q, k, v, d_o, chunk, scale, self.bufs, bwd_order=bwd_order)
+        torch.cuda.current_stream().wait_stream(side)
+
+    def replay(self):
+        self.graph.replay()
+        return self.bufs

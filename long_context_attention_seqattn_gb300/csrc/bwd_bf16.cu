@@ -16,14 +16,17 @@
 // read-modify-write (no other CTA touches those rows in this call, so there is
 // no atomic contention across query tiles).  dQ partial products of every key
 // tile are summed into the zeroed dq with fp32 reductions.
-//   warp 0      TMA producer: K, V once; Q, dO (64 rows) + L, Delta per step
-//   warp 1      TMEM owner + MMA issuer (one thread):
-//                 S^T = K Q^T, dP^T = V dO^T       (M=128 keys, N=64, K=128)
-//                 dV += P^T dO, dK += dS^T Q       (M=128 keys, N=128, K=64)
-//                 dQ^T = K^T dS^T                  (M=128 d,    N=64, K=128)
-//   warps 2..5  P^T, dS^T from TMEM -> bf16 tiles in shared memory; the
-//               final dK/dV read-modify-write
-//   warps 6..9  dQ^T from TMEM -> fp32 reductions into dq
+//   warp 0       TMA producer: K, V once; Q, dO (64 rows) + L, Delta per step
+//                into a 3-stage ring (the load for step n+3 is issued when
+//                step n's MMAs finish, so its latency hides behind two steps)
+//   warp 1       TMEM owner + MMA issuer (one thread):
+//                  S^T = K Q^T, dP^T = V dO^T  (M=128 keys, N=64, K=128; SS)
+//                  dV += P^T dO, dK += dS^T Q  (M=128 keys, N=128, K=64; A in TMEM)
+//                  dQ^T = K^T dS^T             (M=128 d, N=64, K=128; SS)
+//   warps 2..9   P^T, dS^T: two warps per TMEM lane quadrant, 32 query columns
+//                each; P^T/dS^T (bf16) go to TMEM for dV/dK and dS^T also to
+//                shared memory for dQ; the final dK (warps 2-5) / dV (6-9) RMW
+//   warps 10..13 dQ^T from TMEM -> fp32 reductions into dq
 // The next step's S^T/dP^T MMAs are issued before this step's dV/dK/dQ MMAs,
 // so the tensor pipe works while the compute warps form P and dS.
 #include <cuda_bf16.h>
@@ -37,7 +40,9 @@ namespace {
 constexpr int kBK = 128;   // keys per CTA
 constexpr int kBQ = 64;    // query rows per step
 constexpr int kD = 128;    // head dim
-constexpr int kThreads = 320;  // 10 warps
+constexpr int kComputeWarps = 8;                      // two per TMEM lane quadrant
+constexpr int kDQWarp0 = 2 + kComputeWarps;            // 4 dQ warps
+constexpr int kThreads = 32 * (kDQWarp0 + 4);         // 14 warps
 
 constexpr int kKVTileBytes = kBK * kD * 2;         // 32 KB
 constexpr int kKVHalf = kKVTileBytes / 2;          // 16 KB: 128 rows x 128 B
@@ -48,13 +53,13 @@ constexpr int kPTileBytes = kBK * kBQ * 2;         // 16 KB: 128 keys x 64 q
 // shared memory carve-up (bytes from the 1024-aligned base)
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kKVTileBytes;
-constexpr int kOffQ = kOffV + kKVTileBytes;              // 2 stages
-constexpr int kOffDO = kOffQ + 2 * kQTileBytes;          // 2 stages
-constexpr int kOffP = kOffDO + 2 * kQTileBytes;          // 2 buffers
-constexpr int kOffDS = kOffP + 2 * kPTileBytes;          // 2 buffers
-constexpr int kOffStat = kOffDS + 2 * kPTileBytes;       // 2 stages x (L[64], Delta[64])
+constexpr int kQStages = 3;                              // Q/dO/L/Delta ring depth
+constexpr int kOffQ = kOffV + kKVTileBytes;              // kQStages stages
+constexpr int kOffDO = kOffQ + kQStages * kQTileBytes;   // kQStages stages
+constexpr int kOffDS = kOffDO + kQStages * kQTileBytes;  // 2 buffers
+constexpr int kOffStat = kOffDS + 2 * kPTileBytes;       // kQStages x (L[64], Delta[64])
 constexpr int kStatBytes = 2 * kBQ * 4;
-constexpr int kSmemBytes = kOffStat + 2 * kStatBytes;
+constexpr int kSmemBytes = kOffStat + kQStages * kStatBytes;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
 
 constexpr uint32_t kTmemCols = 512;
@@ -63,6 +68,8 @@ constexpr uint32_t kColDV = 128;
 constexpr uint32_t kColS = 256;
 constexpr uint32_t kColDP = 320;
 constexpr uint32_t kColDQ = 384;
+constexpr uint32_t kColPT = 448;   // P^T as bf16 pairs (32 columns), A operand of dV
+constexpr uint32_t kColDST = 480;  // dS^T as bf16 pairs (32 columns), A operand of dK
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -83,10 +90,11 @@ struct BwdParams {
 
 struct BwdBarriers {
   uint64_t kv_full;
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[kQStages], q_empty[kQStages];
   uint64_t sdp_full;
   uint64_t ds_full[2], ds_empty[2];
   uint64_t dq_full, dq_empty;
+  uint64_t pds_free;  // dV/dK MMAs of a step done: P^T/dS^T columns reusable
   uint64_t acc_done;
   uint64_t mma_final;
 };
@@ -141,16 +149,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bars.kv_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kQStages; ++i) {
       mbar_init(&bars.q_full[i], 1);
       mbar_init(&bars.q_empty[i], 1);
-      mbar_init(&bars.ds_full[i], 4 * 32);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.ds_full[i], kComputeWarps * 32);
       mbar_init(&bars.ds_empty[i], 1);
     }
     mbar_init(&bars.sdp_full, 1);
     mbar_init(&bars.dq_full, 1);
     mbar_init(&bars.dq_empty, 4 * 32);
     mbar_init(&bars.acc_done, 1);
+    mbar_init(&bars.pds_free, 1);
     mbar_init(&bars.mma_final, 1);
     fence_barrier_init();
   }
@@ -166,7 +177,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sV = smem_u32(smem + kOffV);
   const uint32_t sQ = smem_u32(smem + kOffQ);
   const uint32_t sDO = smem_u32(smem + kOffDO);
-  const uint32_t sP = smem_u32(smem + kOffP);
   const uint32_t sDS = smem_u32(smem + kOffDS);
   float* stat = reinterpret_cast<float*>(smem + kOffStat);  // [stage][L 64 | Delta 64]
 
@@ -186,10 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(smem + kOffK + kKVHalf, &map_k, &bars.kv_full, 64, g, krow);
       tma_load_3d(smem + kOffV, &map_v, &bars.kv_full, 0, g, krow);
       tma_load_3d(smem + kOffV + kKVHalf, &map_v, &bars.kv_full, 64, g, krow);
-      int issued[2] = {0, 0};
+      int issued[kQStages] = {};
       for (int n = 0; n < n_steps; ++n) {
-        const int st = n & 1;
-        const uint32_t ph = (n >> 1) & 1;
+        const int st = n % kQStages;
+        const uint32_t ph = (n / kQStages) & 1;
         const int h = step_head(n);
         const int qi = step_qtile(n);
         if (!wd.wait(&bars.q_empty[st], ph ^ 1)) break;
@@ -206,8 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (wd.aborted()) {
         wd.drain(&bars.kv_full, 0, 1000000);
-        for (int st = 0; st < 2; ++st)
-          if (issued[st] > 0) wd.drain(&bars.q_full[st], ((issued[st] - 1) >> 1) & 1, 1000000);
+        for (int st = 0; st < kQStages; ++st)
+          if (issued[st] > 0) wd.drain(&bars.q_full[st], ((issued[st] - 1) / kQStages) & 1, 1000000);
       }
     }
   } else if (warp == 1) {
@@ -217,8 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_kv = make_idesc_bf16(kBK, kD, false, true);     // M128 N128, B MN-major
       const uint32_t idesc_dq = make_idesc_bf16(kD, kBQ, true, true);      // M128 N64, both MN-major
       auto issue_sdp = [&](int n) -> bool {
-        const int st = n & 1;
-        if (!wd.wait(&bars.q_full[st], (n >> 1) & 1)) return false;
+        const int st = n % kQStages;
+        if (!wd.wait(&bars.q_full[st], (n / kQStages) & 1)) return false;
         tc_fence_after_sync();
         const uint32_t qa = sQ + st * kQTileBytes;
         const uint32_t da = sDO + st * kQTileBytes;
@@ -234,20 +244,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto issue_grads = [&](int n) -> bool {
-        const int st = n & 1;
+        const int st = n % kQStages;
+        const int db = n & 1;
         const uint32_t qa = sQ + st * kQTileBytes;
         const uint32_t da = sDO + st * kQTileBytes;
-        const uint32_t pa = sP + st * kPTileBytes;
-        const uint32_t dsa = sDS + st * kPTileBytes;
-        // dV += P^T dO ; dK += dS^T Q   (K = 64 query rows: 4 steps)
+        const uint32_t dsa = sDS + db * kPTileBytes;
+        // dV += P^T dO ; dK += dS^T Q   (A from TMEM; K = 64 query rows: 4 steps)
 #pragma unroll
         for (int ks = 0; ks < kBQ / 16; ++ks)
-          umma_bf16_ss(tmem + kColDV, kmajor(pa, kPTileBytes, ks), mnmajor(da, kQHalf, ks), idesc_kv,
+          umma_bf16_ts(tmem + kColDV, tmem + kColPT + ks * 8, mnmajor(da, kQHalf, ks), idesc_kv,
                        (n > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
         for (int ks = 0; ks < kBQ / 16; ++ks)
-          umma_bf16_ss(tmem + kColDK, kmajor(dsa, kPTileBytes, ks), mnmajor(qa, kQHalf, ks), idesc_kv,
+          umma_bf16_ts(tmem + kColDK, tmem + kColDST + ks * 8, mnmajor(qa, kQHalf, ks), idesc_kv,
                        (n > 0 || ks > 0) ? 1u : 0u);
+        umma_commit(&bars.pds_free);
         // dQ^T = K^T dS^T  (K = 128 keys: 8 steps); the dQ warps must have
         // drained the previous step's dQ^T
         if (n >= 1 && !wd.wait(&bars.dq_empty, (n - 1) & 1)) return false;
@@ -258,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        ks > 0 ? 1u : 0u);
         umma_commit(&bars.dq_full);
         umma_commit(&bars.q_empty[st]);
-        umma_commit(&bars.ds_empty[st]);
+        umma_commit(&bars.ds_empty[db]);
         return true;
       };
       bool ok = wd.wait(&bars.kv_full, 0);
@@ -273,97 +284,104 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(&bars.mma_final);
       wd.drain(&bars.mma_final, 0, 4000000);
     }
-  } else if (warp < 6) {
+  } else if (warp < 2 + kComputeWarps) {
     // ------------------------------------------------------------ P / dS
+    // Two warps per TMEM lane quadrant: warp half h owns query columns
+    // [32h, 32h + 32) of every step, so each thread forms 32 P and 32 dS.
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int kr = quad * 32 + lane;                    // key row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const int key = kb + kr;
+    const int c_off = half * 32;                        // first query column of this warp
     bool ok = true;
     for (int n = 0; n < n_steps; ++n) {
-      const int st = n & 1;
+      const int st = n % kQStages;
+      const int db = n & 1;
       const int qi = step_qtile(n);
       if (!(ok = warp_wait(wd, &bars.sdp_full, n & 1))) break;
-      if (!(ok = warp_wait(wd, &bars.q_full[st], (n >> 1) & 1))) break;
-      if (n >= 2 && !(ok = warp_wait(wd, &bars.ds_empty[st], ((n - 2) >> 1) & 1))) break;
+      if (!(ok = warp_wait(wd, &bars.q_full[st], (n / kQStages) & 1))) break;
+      if (n >= 2 && !(ok = warp_wait(wd, &bars.ds_empty[db], ((n - 2) >> 1) & 1))) break;
       tc_fence_after_sync();
-      const float* L = stat + st * 2 * kBQ;
-      const float* Dl = L + kBQ;
+      uint32_t rs[32], rp[32];
+      tmem_ld32(tmem + lane_base + kColS + c_off, rs);
+      tmem_ld32(tmem + lane_base + kColDP + c_off, rp);
+      const float4* L4 = reinterpret_cast<const float4*>(stat + st * 2 * kBQ + c_off);
+      const float4* D4 = reinterpret_cast<const float4*>(stat + st * 2 * kBQ + kBQ + c_off);
+      float lse2[32], dl[32];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 l = L4[j], dd = D4[j];
+        lse2[4 * j] = -l.x * kLog2e; lse2[4 * j + 1] = -l.y * kLog2e;
+        lse2[4 * j + 2] = -l.z * kLog2e; lse2[4 * j + 3] = -l.w * kLog2e;
+        dl[4 * j] = dd.x; dl[4 * j + 1] = dd.y; dl[4 * j + 2] = dd.z; dl[4 * j + 3] = dd.w;
+      }
       const bool masked = diag_tile && (qi - qi_first) < 2;
-      const int q_abs0 = p.q_start + qi * kBQ;          // absolute row of query column 0
-      uint32_t pk[kBQ / 2];                             // P^T row, packed bf16 pairs
-      float pf[kBQ];
+      const int q_abs0 = p.q_start + qi * kBQ + c_off;  // absolute row of this warp's column 0
+      tmem_ld_wait();
+      uint32_t pp[16], pk[16];                          // packed bf16 pairs of P^T and dS^T
 #pragma unroll
-      for (int c0 = 0; c0 < kBQ; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + kColS + c0, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int c = c0 + j;
-          float pv = ex2(fmaf(__uint_as_float(r[j]), p.scale_log2, -L[c] * kLog2e));
-          if (masked && key > q_abs0 + c) pv = 0.f;
-          pf[c] = pv;
+      for (int j = 0; j < 32; j += 2) {
+        float p0 = ex2(fmaf(__uint_as_float(rs[j]), p.scale_log2, lse2[j]));
+        float p1 = ex2(fmaf(__uint_as_float(rs[j + 1]), p.scale_log2, lse2[j + 1]));
+        if (masked) {
+          if (key > q_abs0 + j) p0 = 0.f;
+          if (key > q_abs0 + j + 1) p1 = 0.f;
         }
+        pp[j / 2] = pack_bf16x2(p0, p1);
+        pk[j / 2] = pack_bf16x2(p0 * (__uint_as_float(rp[j]) - dl[j]),
+                                p1 * (__uint_as_float(rp[j + 1]) - dl[j + 1]));
       }
-#pragma unroll
-      for (int c0 = 0; c0 < kBQ; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + kColDP + c0, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const int c = c0 + j;
-          pk[c / 2] = pack_bf16x2(pf[c] * (__uint_as_float(r[j]) - Dl[c]),
-                                  pf[c + 1] * (__uint_as_float(r[j + 1]) - Dl[c + 1]));
-        }
-      }
-      // rows of 64 bf16 = 128 B, 128-byte swizzle inside 8-row groups
+      // dS^T row segment to shared memory (B operand of dQ^T): 128-byte rows,
+      // 128-byte swizzle inside 8-row groups; this warp writes 16-byte chunks
+      // 4*half .. 4*half+3 of its rows
       const uint32_t sw = static_cast<uint32_t>(kr & 7);
-      const uint32_t prow = sP + st * kPTileBytes + kr * 128;
-      const uint32_t dsrow = sDS + st * kPTileBytes + kr * 128;
+      const uint32_t dsrow = sDS + db * kPTileBytes + kr * 128;
 #pragma unroll
-      for (int ci = 0; ci < 8; ++ci) {
-        const int c = ci * 8;
-        st_shared_v4(prow + ((ci ^ sw) << 4), pack_bf16x2(pf[c], pf[c + 1]), pack_bf16x2(pf[c + 2], pf[c + 3]),
-                     pack_bf16x2(pf[c + 4], pf[c + 5]), pack_bf16x2(pf[c + 6], pf[c + 7]));
-        st_shared_v4(dsrow + ((ci ^ sw) << 4), pk[ci * 4], pk[ci * 4 + 1], pk[ci * 4 + 2], pk[ci * 4 + 3]);
-      }
+      for (int ci = 0; ci < 4; ++ci)
+        st_shared_v4(dsrow + (((4 * half + ci) ^ sw) << 4), pk[ci * 4], pk[ci * 4 + 1], pk[ci * 4 + 2],
+                     pk[ci * 4 + 3]);
+      // P^T and dS^T segments to TMEM (A operands of dV and dK) once the
+      // previous step's dV/dK MMAs have read the old ones
+      if (n >= 1 && !(ok = warp_wait(wd, &bars.pds_free, (n - 1) & 1))) break;
+      tmem_st16(tmem + lane_base + kColPT + 16 * half, pp);
+      tmem_st16(tmem + lane_base + kColDST + 16 * half, pk);
+      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before_sync();
-      mbar_arrive(&bars.ds_full[st]);
+      mbar_arrive(&bars.ds_full[db]);
     }
-    // ---- epilogue: dK, dV rows of this tile into the running sums
+    // ---- epilogue: this tile's dK (half 0) or dV (half 1) rows into the running sums
     if (ok) ok = warp_wait(wd, &bars.acc_done, 0);
     if (ok) {
       tc_fence_after_sync();
       const int64_t row = (static_cast<int64_t>(b) * p.T + key) * p.Hkv + g;
-      float4* dkrow = reinterpret_cast<float4*>(p.dk + row * kD);
-      float4* dvrow = reinterpret_cast<float4*>(p.dv + row * kD);
+      float4* dst = reinterpret_cast<float4*>((half == 0 ? p.dk : p.dv) + row * kD);
+      const uint32_t col = half == 0 ? kColDK : kColDV;
+      const float f = half == 0 ? p.scale : 1.f;
 #pragma unroll
-      for (int c0 = 0; c0 < kD; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + kColDK + c0, r);
+      for (int c0 = 0; c0 < kD; c0 += 64) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tmem + lane_base + col + c0, r0);
+        tmem_ld32(tmem + lane_base + col + c0 + 32, r1);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
-          float4 a = dkrow[(c0 + j) / 4];
-          a.x += p.scale * __uint_as_float(r[j]);
-          a.y += p.scale * __uint_as_float(r[j + 1]);
-          a.z += p.scale * __uint_as_float(r[j + 2]);
-          a.w += p.scale * __uint_as_float(r[j + 3]);
-          dkrow[(c0 + j) / 4] = a;
+          float4 a = dst[(c0 + j) / 4];
+          a.x += f * __uint_as_float(r0[j]);
+          a.y += f * __uint_as_float(r0[j + 1]);
+          a.z += f * __uint_as_float(r0[j + 2]);
+          a.w += f * __uint_as_float(r0[j + 3]);
+          dst[(c0 + j) / 4] = a;
         }
-        tmem_ld32(tmem + lane_base + kColDV + c0, r);
-        tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
-          float4 a = dvrow[(c0 + j) / 4];
-          a.x += __uint_as_float(r[j]);
-          a.y += __uint_as_float(r[j + 1]);
-          a.z += __uint_as_float(r[j + 2]);
-          a.w += __uint_as_float(r[j + 3]);
-          dvrow[(c0 + j) / 4] = a;
+          float4 a = dst[(c0 + 32 + j) / 4];
+          a.x += f * __uint_as_float(r1[j]);
+          a.y += f * __uint_as_float(r1[j + 1]);
+          a.z += f * __uint_as_float(r1[j + 2]);
+          a.w += f * __uint_as_float(r1[j + 3]);
+          dst[(c0 + 32 + j) / 4] = a;
         }
       }
     }

@@ -8,16 +8,23 @@
 //
 // One CTA owns one 128-row query tile of one head and streams the head's
 // key/value tiles [kv_begin, q0 + 128) through shared memory:
-//   warp 0      TMA producer: Q once, then K/V tiles into 2-stage rings
-//   warp 1      TMEM owner + MMA issuer (one thread): S = Q K^T, O += P V
-//   warps 2..5  softmax: S row from TMEM -> online max/sum -> P (bf16) into
-//               shared memory; rare O rescale in TMEM; epilogue O/l, LSE
-// S is double-buffered in TMEM so the next QK^T overlaps this tile's
-// softmax.  Only the last (diagonal) key tile carries the causal mask; the
-// prefix tiles are unmasked.  The running max is rescaled lazily: O and l
-// are only corrected when a row max grows by more than 2^8, which keeps P
-// below 256 (exact in fp32/bf16 range) and skips almost every TMEM
-// read-modify-write of O.
+//   warp 0      TMA producer of Q (once) and K tiles (3-stage ring)
+//   warp 10     TMA producer of V tiles (its own 3-stage ring, so a K load
+//               never queues behind a V slot that frees later)
+//   warp 1      TMEM owner + MMA issuer (one thread): S = Q K^T (SS),
+//               O_h += P_h V_h (A operand P_h read from TMEM)
+//   warps 2..9  softmax, two warps per TMEM lane quadrant
+// Each key tile is split in two 64-key halves; softmax warp half h owns keys
+// [64h, 64h + 64) of every tile for its 32 rows, with its own running max and
+// sum and its own output accumulator O_h = sum P_h V_h in TMEM.  The two
+// halves are merged once, in the epilogue (O = (O_0 2^m0 + O_1 2^m1) /
+// (l_0 2^m0 + l_1 2^m1)), so the per-tile softmax needs no exchange between
+// warps, and each SM sub-partition runs two softmax warps.  P is written back
+// into TMEM (over the S values just read) and never touches shared memory.
+// TMEM: S double-buffered (2 x 128 columns), O_0 and O_1 (128 columns each).
+// Only the last (diagonal) key tile carries the causal mask.  The running
+// maxima are rescaled lazily: O_h and l_h are only corrected when a row max
+// grows by more than 2^8 (P stays below 256).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -26,22 +33,26 @@
 namespace seqattn {
 namespace {
 
-constexpr int kBM = 128;             // query rows per CTA
-constexpr int kBN = 128;             // keys per tile
-constexpr int kD = 128;              // head dim
-constexpr int kTileBytes = kBM * kD * 2;  // 32 KB: one 128x128 bf16 tile
+constexpr int kBM = 128;                    // query rows per CTA
+constexpr int kBN = 128;                    // keys per tile
+constexpr int kD = 128;                     // head dim
+constexpr int kTileBytes = kBM * kD * 2;    // 32 KB: one 128x128 bf16 tile
 constexpr int kHalfBytes = kTileBytes / 2;  // one 64-column (128-byte) block
-constexpr int kThreads = 192;        // 6 warps
+constexpr int kSoftmaxWarps = 8;
+constexpr int kVWarp = 2 + kSoftmaxWarps;           // V producer warp
+constexpr int kThreads = 32 * (kVWarp + 1);         // 11 warps
+constexpr int kStages = 3;                          // K and V ring depth
 
 // shared memory carve-up (bytes from the 1024-aligned base)
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;        // 2 stages
-constexpr int kOffV = kOffK + 2 * kTileBytes;    // 2 stages
-constexpr int kOffP = kOffV + 2 * kTileBytes;    // 2 buffers
-constexpr int kSmemBytes = kOffP + 2 * kTileBytes;
+constexpr int kOffK = kOffQ + kTileBytes;              // kStages stages
+constexpr int kOffV = kOffK + kStages * kTileBytes;    // kStages stages
+constexpr int kSmemBytes = kOffV + kStages * kTileBytes;
 constexpr int kSmemAlloc = kSmemBytes + 1024;    // + alignment slack
 
-// TMEM columns: S buffers at 0 and 128, O at 256.
+// TMEM columns: S buffers at 0 and 128, O_0 at 256, O_1 at 384.  P of key
+// half h (bf16 pairs, 32 columns) overwrites columns [64h, 64h + 32) of its S
+// buffer once the softmax has read them.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
@@ -63,8 +74,8 @@ struct FwdParams {
 
 struct FwdBarriers {
   uint64_t q_full;
-  uint64_t k_full[2], k_empty[2];
-  uint64_t v_full[2], v_empty[2];
+  uint64_t k_full[kStages], k_empty[kStages];
+  uint64_t v_full[kStages], v_empty[kStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
@@ -118,13 +129,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bars.q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&bars.k_full[i], 1);
       mbar_init(&bars.k_empty[i], 1);
       mbar_init(&bars.v_full[i], 1);
       mbar_init(&bars.v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.p_full[i], 4 * 32);
+      mbar_init(&bars.p_full[i], kSoftmaxWarps * 32);
       mbar_init(&bars.pv_done[i], 1);
     }
     mbar_init(&bars.mma_final, 1);
@@ -141,43 +154,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_u32(smem + kOffQ);
   const uint32_t sK = smem_u32(smem + kOffK);
   const uint32_t sV = smem_u32(smem + kOffV);
-  const uint32_t sP = smem_u32(smem + kOffP);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == kVWarp) {
+    // ------------------------------------------------------------ producers
+    // warp 0 streams Q then K, warp kVWarp streams V, each into its own ring,
+    // so a K tile never waits behind the slower-to-free V slot.
     if (lane == 0) {
-      prefetch_tensormap(&map_q);
-      prefetch_tensormap(&map_k);
-      prefetch_tensormap(&map_v);
-      const int qrow = b * p.q_len + qt * kBM;
-      mbar_arrive_expect_tx(&bars.q_full, kTileBytes);
-      tma_load_3d(smem + kOffQ, &map_q, &bars.q_full, 0, h, qrow);
-      tma_load_3d(smem + kOffQ + kHalfBytes, &map_q, &bars.q_full, 64, h, qrow);
-      int issued[2] = {0, 0};
+      const bool is_k = (warp == 0);
+      const CUtensorMap* map = is_k ? &map_k : &map_v;
+      const int off = is_k ? kOffK : kOffV;
+      uint64_t* full = is_k ? bars.k_full : bars.v_full;
+      uint64_t* empty = is_k ? bars.k_empty : bars.v_empty;
+      prefetch_tensormap(map);
+      if (is_k) {
+        prefetch_tensormap(&map_q);
+        const int qrow = b * p.q_len + qt * kBM;
+        mbar_arrive_expect_tx(&bars.q_full, kTileBytes);
+        tma_load_3d(smem + kOffQ, &map_q, &bars.q_full, 0, h, qrow);
+        tma_load_3d(smem + kOffQ + kHalfBytes, &map_q, &bars.q_full, 64, h, qrow);
+      }
+      int issued[kStages] = {};
       for (int t = 0; t < n_kv; ++t) {
-        const int st = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
+        const int st = t % kStages;
+        const uint32_t ph = (t / kStages) & 1;
         const int krow = b * p.T + p.kv_begin + t * kBN;
-        if (!wd.wait(&bars.k_empty[st], ph ^ 1)) break;
-        mbar_arrive_expect_tx(&bars.k_full[st], kTileBytes);
-        tma_load_3d(smem + kOffK + st * kTileBytes, &map_k, &bars.k_full[st], 0, g, krow);
-        tma_load_3d(smem + kOffK + st * kTileBytes + kHalfBytes, &map_k, &bars.k_full[st], 64, g, krow);
-        if (!wd.wait(&bars.v_empty[st], ph ^ 1)) { issued[st] = t + 1; break; }
-        mbar_arrive_expect_tx(&bars.v_full[st], kTileBytes);
-        tma_load_3d(smem + kOffV + st * kTileBytes, &map_v, &bars.v_full[st], 0, g, krow);
-        tma_load_3d(smem + kOffV + st * kTileBytes + kHalfBytes, &map_v, &bars.v_full[st], 64, g, krow);
+        if (!wd.wait(&empty[st], ph ^ 1)) break;
+        mbar_arrive_expect_tx(&full[st], kTileBytes);
+        tma_load_3d(smem + off + st * kTileBytes, map, &full[st], 0, g, krow);
+        tma_load_3d(smem + off + st * kTileBytes + kHalfBytes, map, &full[st], 64, g, krow);
         issued[st] = t + 1;
       }
       if (wd.aborted()) {
         // let copies already in flight land before the CTA's smem goes away
-        wd.drain(&bars.q_full, 0, 1000000);
-        for (int st = 0; st < 2; ++st) {
-          if (issued[st] > 0) {
-            const uint32_t ph = ((issued[st] - 1) >> 1) & 1;
-            wd.drain(&bars.k_full[st], ph, 1000000);
-            wd.drain(&bars.v_full[st], ph, 1000000);
-          }
-        }
+        if (is_k) wd.drain(&bars.q_full, 0, 1000000);
+        for (int st = 0; st < kStages; ++st)
+          if (issued[st] > 0) wd.drain(&full[st], ((issued[st] - 1) / kStages) & 1, 1000000);
       }
     }
   } else if (warp == 1) {
@@ -187,33 +198,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_o = make_idesc_bf16(kBM, kD, false, true);
       bool ok = wd.wait(&bars.q_full, 0);
       auto issue_pv = [&](int u) -> bool {
-        const int su = u & 1;
-        const uint32_t phu = (u >> 1) & 1;
-        if (!wd.wait(&bars.v_full[su], phu)) return false;
-        if (!wd.wait(&bars.p_full[su], phu)) return false;
+        const int vs = u % kStages;
+        if (!wd.wait(&bars.v_full[vs], (u / kStages) & 1)) return false;
+        if (!wd.wait(&bars.p_full[u & 1], (u >> 1) & 1)) return false;
         tc_fence_after_sync();
-        const uint32_t pa = sP + su * kTileBytes;
-        const uint32_t va = sV + su * kTileBytes;
+        const uint32_t va = sV + vs * kTileBytes;
+        const uint32_t pa = tmem + kColS + (u & 1) * kBN;   // P in the S buffer, lane 0
+        // O_h += P_h V[64h:64h+64, :] with P_h (bf16 pairs) at columns [64h, 64h+32)
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks)
-          umma_bf16_ss(tmem + kColO, kmajor_desc(pa, ks), v_mn_desc(va, ks), idesc_o,
-                       (u > 0 || ks > 0) ? 1u : 0u);
-        umma_commit(&bars.pv_done[su]);
-        umma_commit(&bars.v_empty[su]);
+          umma_bf16_ts(tmem + kColO + (ks >> 2) * 128, pa + (ks >> 2) * 64 + (ks & 3) * 8,
+                       v_mn_desc(va, ks), idesc_o, (u > 0 || (ks & 3) > 0) ? 1u : 0u);
+        umma_commit(&bars.pv_done[u & 1]);
+        umma_commit(&bars.v_empty[vs]);
         return true;
       };
       for (int t = 0; ok && t < n_kv; ++t) {
-        const int st = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
-        if (!(ok = wd.wait(&bars.k_full[st], ph))) break;
+        const int ks_st = t % kStages;
+        if (!(ok = wd.wait(&bars.k_full[ks_st], (t / kStages) & 1))) break;
         tc_fence_after_sync();
-        const uint32_t ka = sK + st * kTileBytes;
+        const uint32_t ka = sK + ks_st * kTileBytes;
+        // S(t) overwrites P(t-2) in buffer t&1: PV(t-2) was issued earlier and
+        // tcgen05 MMAs of one thread execute in issue order
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks)
-          umma_bf16_ss(tmem + kColS + st * kBN, kmajor_desc(sQ, ks), kmajor_desc(ka, ks), idesc_s,
+          umma_bf16_ss(tmem + kColS + (t & 1) * kBN, kmajor_desc(sQ, ks), kmajor_desc(ka, ks), idesc_s,
                        ks > 0 ? 1u : 0u);
-        umma_commit(&bars.s_full[st]);
-        umma_commit(&bars.k_empty[st]);
+        umma_commit(&bars.s_full[t & 1]);
+        umma_commit(&bars.k_empty[ks_st]);
         if (t >= 1) ok = issue_pv(t - 1);
       }
       if (ok) issue_pv(n_kv - 1);
@@ -224,9 +236,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ softmax
     const int quad = warp & 3;                   // TMEM lane quadrant of this warp
+    const int half = (warp - 2) >> 2;            // key half of every tile
     const int row = quad * 32 + lane;            // query row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    float m_run = -INFINITY;                     // running max, log2 units
+    const uint32_t colO = tmem + lane_base + kColO + half * 128;
+    const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
+    float m_run = -INFINITY;                     // running max of this half, log2 units
     float l_run = 0.f;
     bool ok = true;
     for (int t = 0; t < n_kv; ++t) {
@@ -234,68 +249,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ph = (t >> 1) & 1;
       if (!(ok = warp_wait(wd, &bars.s_full[st], ph))) break;
       tc_fence_after_sync();
-      float s[kBN];
-#pragma unroll
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + kColS + st * kBN + c0, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) s[c0 + j] = __uint_as_float(r[j]) * p.scale_log2;
-      }
-      if (t == n_kv - 1) {
+      uint32_t ra[32], rb[32];                   // scores of keys 64h .. 64h+63
+      tmem_ld32(tmem + lane_base + kColS + st * kBN + half * 64, ra);
+      tmem_ld32(tmem + lane_base + kColS + st * kBN + half * 64 + 32, rb);
+      tmem_ld_wait();
+      const bool diag = (t == n_kv - 1);
+      if (diag) {
         // diagonal tile: key c (absolute q0 + c) is visible to row r iff c <= r
 #pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (c > row) s[c] = -INFINITY;
+        for (int j = 0; j < 32; ++j) {
+          if (half * 64 + j > row) ra[j] = __float_as_uint(-INFINITY);
+          if (half * 64 + 32 + j > row) rb[j] = __float_as_uint(-INFINITY);
+        }
       }
-      float mx = s[0];
+      float mx = fmax3(__uint_as_float(ra[0]), __uint_as_float(ra[1]), __uint_as_float(rb[0]));
 #pragma unroll
-      for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+      for (int j = 1; j < 16; ++j)
+        mx = fmax3(mx, __uint_as_float(ra[2 * j]), __uint_as_float(ra[2 * j + 1]));
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (j == 0) mx = fmaxf(mx, __uint_as_float(rb[1]));
+        else mx = fmax3(mx, __uint_as_float(rb[2 * j]), __uint_as_float(rb[2 * j + 1]));
+      }
+      mx *= p.scale_log2;                        // -inf stays -inf: no visible key in this half yet
       const bool need = mx > m_run + kRescaleThreshold;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? mx : m_run;
-        const float alpha = ex2(m_run - m_new);  // 0 on the first tile, 1 if !need
+        const float alpha = need ? ex2(m_run - m_new) : 1.f;  // 0 on the first visible tile
         l_run *= alpha;
         m_run = m_new;
         if (t > 0) {
-          // O holds PV_0..PV_{t-1}: wait for PV_{t-1}, then scale O by alpha
+          // O_h holds PV_0..PV_{t-1}: wait for PV_{t-1}, then scale O_h by alpha
           const int u = t - 1;
           if (!(ok = warp_wait(wd, &bars.pv_done[u & 1], (u >> 1) & 1))) break;
           tc_fence_after_sync();
 #pragma unroll
-          for (int c0 = 0; c0 < kD; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_base + kColO + c0, r);
+          for (int c0 = 0; c0 < kD; c0 += 64) {
+            uint32_t r0[32], r1[32];
+            tmem_ld32(colO + c0, r0);
+            tmem_ld32(colO + c0 + 32, r1);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-            tmem_st32(tmem + lane_base + kColO + c0, r);
+            for (int j = 0; j < 32; ++j) {
+              r0[j] = __float_as_uint(__uint_as_float(r0[j]) * alpha);
+              r1[j] = __float_as_uint(__uint_as_float(r1[j]) * alpha);
+            }
+            tmem_st32(colO + c0, r0);
+            tmem_st32(colO + c0 + 32, r1);
           }
           tmem_st_wait();
         }
       }
-      // P buffer st was last read by PV_{t-2}
-      if (t >= 2) {
-        const int u = t - 2;
-        if (!(ok = warp_wait(wd, &bars.pv_done[u & 1], (u >> 1) & 1))) break;
-      }
-      const uint32_t prow = sP + st * kTileBytes + row * 128;
-      const uint32_t sw = static_cast<uint32_t>(row & 7);
+      // P = 2^(s * scale * log2e - m) for this row's 64 keys -> bf16 pairs ->
+      // TMEM columns [64h, 64h + 32) of the S buffer (already read above)
+      const uint64_t negm = f2_pack(-m_run, -m_run);
+      const bool live = m_run != -INFINITY;      // a half with no visible key yet writes zeros
+      uint64_t lsum = f2_pack(0.f, 0.f);
+      uint32_t pw[32];
 #pragma unroll
-      for (int ci = 0; ci < kBN / 8; ++ci) {
-        const int c = ci * 8;
-        float e[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          e[j] = ex2(s[c + j] - m_run);
-          l_run += e[j];
-        }
-        const uint32_t addr = prow + (ci >> 3) * kHalfBytes + (((ci & 7) ^ sw) << 4);
-        st_shared_v4(addr, pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
-                     pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+      for (int k2 = 0; k2 < 32; ++k2) {
+        const uint32_t* src = k2 < 16 ? &ra[2 * k2] : &rb[2 * (k2 - 16)];
+        const uint64_t x = f2_fma(f2_pack(__uint_as_float(src[0]), __uint_as_float(src[1])), scale2, negm);
+        float a, c;
+        f2_unpack(x, a, c);
+        const float ea = live ? ex2(a) : 0.f;
+        const float ec = live ? ex2(c) : 0.f;
+        lsum = f2_add(lsum, f2_pack(ea, ec));
+        pw[k2] = pack_bf16x2(ea, ec);
       }
-      fence_proxy_async_smem();
+      {
+        float a, c;
+        f2_unpack(lsum, a, c);
+        l_run += a + c;
+      }
+      tmem_st32(tmem + lane_base + kColS + st * kBN + half * 64, pw);
+      tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(&bars.p_full[st]);
     }
@@ -303,27 +331,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = n_kv - 1;
       ok = warp_wait(wd, &bars.pv_done[u & 1], (u >> 1) & 1);
     }
-    if (ok) {
+    // ---- epilogue: merge the two halves of every row.  The exchange uses the
+    // K ring, idle once the last PV product has completed.
+    float (*merge_m)[kBM] = reinterpret_cast<float (*)[kBM]>(smem + kOffK);
+    float (*merge_l)[kBM] = reinterpret_cast<float (*)[kBM]>(smem + kOffK + 2 * kBM * 4);
+    merge_m[half][row] = m_run;
+    merge_l[half][row] = l_run;
+    named_barrier_sync(1, kSoftmaxWarps * 32);
+    if (ok && !wd.aborted()) {
       tc_fence_after_sync();
-      const float inv = 1.f / l_run;
+      const float m0 = merge_m[0][row], m1 = merge_m[1][row];
+      const float M = fmaxf(m0, m1);
+      const float a0 = m0 == -INFINITY ? 0.f : ex2(m0 - M);
+      const float a1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
+      const float L = merge_l[0][row] * a0 + merge_l[1][row] * a1;
+      const float inv = 1.f / L;
+      const float f0 = a0 * inv, f1 = a1 * inv;
       const int qrow = qt * kBM + row;
-      uint4* orow = reinterpret_cast<uint4*>(p.o + ((static_cast<int64_t>(b) * p.q_len + qrow) * p.Hq + h) * kD);
+      // this warp writes head-dim columns [64 half, 64 half + 64) of the row
+      uint4* orow = reinterpret_cast<uint4*>(p.o + ((static_cast<int64_t>(b) * p.q_len + qrow) * p.Hq + h) * kD +
+                                             half * 64);
 #pragma unroll
-      for (int c0 = 0; c0 < kD; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + kColO + c0, r);
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tmem + lane_base + kColO + half * 64 + c0, r0);
+        tmem_ld32(tmem + lane_base + kColO + 128 + half * 64 + c0, r1);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; j += 8) {
-          uint4 v;
-          v.x = pack_bf16x2(__uint_as_float(r[j + 0]) * inv, __uint_as_float(r[j + 1]) * inv);
-          v.y = pack_bf16x2(__uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
-          v.z = pack_bf16x2(__uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv);
-          v.w = pack_bf16x2(__uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv);
-          orow[(c0 + j) / 8] = v;
+          float v[8];
+#pragma unroll
+          for (int k2 = 0; k2 < 8; ++k2)
+            v[k2] = __uint_as_float(r0[j + k2]) * f0 + __uint_as_float(r1[j + k2]) * f1;
+          uint4 q;
+          q.x = pack_bf16x2(v[0], v[1]);
+          q.y = pack_bf16x2(v[2], v[3]);
+          q.z = pack_bf16x2(v[4], v[5]);
+          q.w = pack_bf16x2(v[6], v[7]);
+          orow[(c0 + j) / 8] = q;
         }
       }
-      p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.q_len + qrow] = (m_run + __log2f(l_run)) * kLn2;
+      if (half == 0)
+        p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.q_len + qrow] = (M + __log2f(L)) * kLn2;
     }
   }
 
