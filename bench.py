@@ -31,9 +31,9 @@ UNIT = "TFLOP/s"
 FALLBACK_SUSTAINED_TFLOPS = 1700.0   # used only when no measured peaks file exists
 
 # DRAM traffic (bytes read + written) per backward launch, from the ncu
-# capture summarised under profiles/ (average over the 16 chunk launches of the
-# bench workload); set to None whenever the kernel changes until re-measured.
-BWD_TRAFFIC_BYTES_PER_LAUNCH = 401.3e6   # bwd_bf16_kernel, 3-stage ring (launches_llama3-8b-layer-t32768-c2048.md)
+# launch list of the bench workload (average over its 16 chunk launches);
+# set to None whenever the kernel changes until it is measured again.
+BWD_TRAFFIC_BYTES_PER_LAUNCH = 401.3e6   # bwd_bf16_kernel with the 3-stage Q/dO ring
 
 
 def parse_args():
