@@ -279,3 +279,95 @@ class LayerGraph:
     def replay(self):
         self.graph.replay()
         return self.bufs
+
+
+class HostLayerPass:
+    """A layer pass whose inputs start and whose outputs end in pinned host
+    memory, with the transfers overlapped with the chunk calls.
+
+    Forward chunk i needs only query rows of chunk i and key/value rows
+    [0, end of chunk i), so inputs are uploaded chunk by chunk ahead of the
+    forward calls.  With the last-to-first backward order (the relay order
+    of SeCO's Algorithm 2), the dK/dV rows of chunk j receive their last
+    contribution from chunk j's backward, so every output chunk (O, LSE, dQ,
+    dK, dV rows) is copied back as soon as it is final, while later chunks
+    still compute.  Two side streams carry the copies; CUDA events order
+    them against the compute stream."""
+
+    def __init__(self, h_q, h_k, h_v, h_do, chunk, device="cuda"):
+        B, T, Hq, d = h_q.shape
+        if B != 1:
+            raise ValueError("HostLayerPass streams row ranges of B=1 tensors")
+        self.h_in = (h_q, h_k, h_v, h_do)
+        self.chunk = chunk
+        self.d_in = tuple(torch.empty(x.shape, dtype=x.dtype, device=device) for x in self.h_in)
+        self.bufs = LayerBuffers(self.d_in[0], self.d_in[1], chunk)
+        self.h_o = torch.empty(h_q.shape, dtype=h_q.dtype, pin_memory=True)
+        self.h_lse = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in self.bufs.lse_chunks]
+        self.h_dq = torch.empty(h_q.shape, dtype=torch.float32, pin_memory=True)
+        self.h_dk = torch.empty(h_k.shape, dtype=torch.float32, pin_memory=True)
+        self.h_dv = torch.empty(h_k.shape, dtype=torch.float32, pin_memory=True)
+        self.up = torch.cuda.Stream()
+        self.down = torch.cuda.Stream()
+
+    def bytes_moved(self):
+        h2d = sum(x.numel() * x.element_size() for x in self.h_in)
+        d2h = sum(x.numel() * x.element_size() for x in (self.h_o, self.h_dq, self.h_dk, self.h_dv))
+        d2h += sum(x.numel() * x.element_size() for x in self.h_lse)
+        return h2d, d2h
+
+    def run(self):
+        """Enqueue one pass on the current stream (copies on side streams).
+        Returns the host output tensors (valid after the stream syncs)."""
+        main = torch.cuda.current_stream()
+        q, k, v, do = self.d_in
+        h_q, h_k, h_v, h_do = self.h_in
+        b = self.bufs
+        T, c = q.shape[1], self.chunk
+        starts = b.starts
+        self.up.wait_stream(main)
+        self.down.wait_stream(main)
+        ev_in, ev_do = [], []
+        with torch.cuda.stream(self.up):
+            for s in starts:
+                e = min(s + c, T)
+                for dst, src in ((q, h_q), (k, h_k), (v, h_v)):
+                    dst[:, s:e].copy_(src[:, s:e], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(self.up)
+                ev_in.append(ev)
+            for s in starts:
+                e = min(s + c, T)
+                do[:, s:e].copy_(h_do[:, s:e], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(self.up)
+                ev_do.append(ev)
+        reset_accum(b.dk, b.dv, q.shape[2], main)
+        for i, s in enumerate(starts):
+            e = min(s + c, T)
+            main.wait_event(ev_in[i])
+            chunk_fwd(_rows(q, s, e), k, v, b.o[:, s:e], b.lse_chunks[i], s, s, None, main)
+            ev = torch.cuda.Event()
+            ev.record(main)
+            self.down.wait_event(ev)
+            with torch.cuda.stream(self.down):
+                self.h_o[:, s:e].copy_(b.o[:, s:e], non_blocking=True)
+                self.h_lse[i].copy_(b.lse_chunks[i], non_blocking=True)
+        for i in range(len(starts) - 1, -1, -1):
+            s = starts[i]
+            e = min(s + c, T)
+            main.wait_event(ev_do[i])
+            chunk_bwd(_rows(q, s, e), k, v, _rows(b.o, s, e), b.lse_chunks[i], _rows(do, s, e),
+                      b.dq[:, s:e], b.dk, b.dv, s, s, None, b.workspace, main)
+            ev = torch.cuda.Event()
+            ev.record(main)
+            self.down.wait_event(ev)
+            with torch.cuda.stream(self.down):
+                # rows of chunk i are final: later chunks (already done) and
+                # this one were the only ones touching them
+                self.h_dq[:, s:e].copy_(b.dq[:, s:e], non_blocking=True)
+                self.h_dk[:, s:e].copy_(b.dk[:, s:e], non_blocking=True)
+                self.h_dv[:, s:e].copy_(b.dv[:, s:e], non_blocking=True)
+        main.wait_stream(self.down)
+        main.wait_stream(self.up)
+        return self.h_o, self.h_lse, self.h_dq, self.h_dk, self.h_dv

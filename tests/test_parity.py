@@ -290,3 +290,22 @@ def test_bf16_graph_replay_matches_eager():
         got = (got_b.o, binding.gather_lse(got_b), got_b.dq, got_b.dk, got_b.dv)
         for name, a, r in zip(("O", "LSE", "dQ", "dK", "dV"), got, ref):
             assert_bf16(f"graph step {step} {name}", cpu64(a), cpu64(r))
+
+
+def test_bf16_host_pass_matches_device_pass():
+    """The host-buffer pass (inputs streamed in chunk by chunk, every output
+    chunk copied back as soon as it is final) returns the device pass."""
+    B, T, Hq, Hkv, d, chunk = 1, 1024, 4, 2, 128, 256
+    cpu = small_inputs(B, T, Hq, Hkv, d, "bf16", 66)
+    pinned = [x.pin_memory() for x in cpu]
+    hp = binding.HostLayerPass(*pinned, chunk)
+    for _ in range(2):
+        h_o, h_lse, h_dq, h_dk, h_dv = hp.run()
+        torch.cuda.synchronize()
+        binding.sync_status()
+        ref = run_layer(*[x.cuda() for x in cpu], chunk)
+        assert_bf16("O", h_o.double().numpy(), cpu64(ref.o))
+        assert_bf16("LSE", torch.cat(h_lse, dim=2).double().numpy(), cpu64(binding.gather_lse(ref)))
+        assert_bf16("dQ", h_dq.double().numpy(), cpu64(ref.dq))
+        assert_bf16("dK", h_dk.double().numpy(), cpu64(ref.dk))
+        assert_bf16("dV", h_dv.double().numpy(), cpu64(ref.dv))
