@@ -11,8 +11,10 @@
 //   warp 0      TMA producer of Q (once) and K tiles (3-stage ring)
 //   warp 10     TMA producer of V tiles (its own 3-stage ring, so a K load
 //               never queues behind a V slot that frees later)
-//   warp 1      TMEM owner + MMA issuer (one thread): S = Q K^T (SS),
-//               O_h += P_h V_h (A operand P_h read from TMEM)
+//   warp 1      TMEM owner + MMA issuer of S = Q K^T (SS)
+//   warp 11     MMA issuer of O_h += P_h V_h (A operand P_h read from TMEM);
+//               two issuing threads because one thread keeps only about one
+//               tcgen05.mma in flight per ~90 cycles
 //   warps 2..9  softmax, two warps per TMEM lane quadrant
 // Each key tile is split in two 64-key halves; softmax warp half h owns keys
 // [64h, 64h + 64) of every tile for its 32 rows, with its own running max and
@@ -40,7 +42,8 @@ constexpr int kTileBytes = kBM * kD * 2;    // 32 KB: one 128x128 bf16 tile
 constexpr int kHalfBytes = kTileBytes / 2;  // one 64-column (128-byte) block
 constexpr int kSoftmaxWarps = 8;
 constexpr int kVWarp = 2 + kSoftmaxWarps;           // V producer warp
-constexpr int kThreads = 32 * (kVWarp + 1);         // 11 warps
+constexpr int kPVWarp = kVWarp + 1;                 // second MMA issuer (PV)
+constexpr int kThreads = 32 * (kPVWarp + 1);        // 12 warps
 constexpr int kStages = 3;                          // K and V ring depth
 
 // shared memory carve-up (bytes from the 1024-aligned base)
@@ -79,7 +82,7 @@ struct FwdBarriers {
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
-  uint64_t mma_final;
+  uint64_t mma_final[2];
 };
 
 // All 32 lanes wait; the warp proceeds only if every lane saw the phase, so
@@ -89,17 +92,19 @@ __device__ __forceinline__ bool warp_wait(Watchdog& wd, uint64_t* bar, uint32_t 
   return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_addr, int ks) {
-  // K-major 128x128 bf16 tile = two 64-column blocks of 128 rows x 128 B.
-  // K-step ks (16 elements) -> block ks/4, byte offset 32*(ks%4) in the row.
-  return make_desc_sw128(tile_addr + (ks >> 2) * kHalfBytes + (ks & 3) * 32, 16, 1024);
+// Shared-memory descriptors are built once per tile base; a K-step moves only
+// the 14-bit start-address field (16-byte units), so each MMA's operands are
+// the base plus a compile-time constant -- building the full descriptor in
+// front of every MMA would put a serial integer chain on the issuing thread.
+// K-major 128x128 bf16 tile = two 64-column blocks of 128 rows x 128 B;
+// K-step ks (16 elements) -> block ks/4, byte offset 32*(ks%4) in the row.
+__host__ __device__ constexpr uint32_t kmajor_off(int ks) {
+  return static_cast<uint32_t>(((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4);
 }
-
-__device__ __forceinline__ uint64_t v_mn_desc(uint32_t tile_addr, int ks) {
-  // V tile [128 keys][128 d] used as the MN-major B operand (N = d, K = keys):
-  // 8-key groups of 1024 B along K, the two 64-wide d blocks 16 KB apart.
-  return make_desc_sw128(tile_addr + ks * 2048, kHalfBytes, 1024);
-}
+// V tile [128 keys][128 d] as the MN-major B operand (N = d, K = keys):
+// 8-key groups of 1024 B along K, the two 64-wide d blocks 16 KB apart.
+__host__ __device__ constexpr uint32_t vmn_off(int ks) { return static_cast<uint32_t>((ks * 2048) >> 4); }
+constexpr uint32_t kTileUnits = kTileBytes >> 4;
 
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -140,7 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.p_full[i], kSoftmaxWarps * 32);
       mbar_init(&bars.pv_done[i], 1);
     }
-    mbar_init(&bars.mma_final, 1);
+    mbar_init(&bars.mma_final[0], 1);
+    mbar_init(&bars.mma_final[1], 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -191,47 +197,57 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (issued[st] > 0) wd.drain(&full[st], ((issued[st] - 1) / kStages) & 1, 1000000);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kPVWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    // warp 1 issues the S = Q K^T products, warp kPVWarp the O_h += P_h V_h
+    // products.  Their only shared TMEM columns are the S buffers: S(t)
+    // overwrites P(t-2), so S(t) waits for PV(t-2) to complete.
     if (lane == 0) {
       const uint32_t idesc_s = make_idesc_bf16(kBM, kBN, false, false);
       const uint32_t idesc_o = make_idesc_bf16(kBM, kD, false, true);
-      bool ok = wd.wait(&bars.q_full, 0);
-      auto issue_pv = [&](int u) -> bool {
-        const int vs = u % kStages;
-        if (!wd.wait(&bars.v_full[vs], (u / kStages) & 1)) return false;
-        if (!wd.wait(&bars.p_full[u & 1], (u >> 1) & 1)) return false;
-        tc_fence_after_sync();
-        const uint32_t va = sV + vs * kTileBytes;
-        const uint32_t pa = tmem + kColS + (u & 1) * kBN;   // P in the S buffer, lane 0
-        // O_h += P_h V[64h:64h+64, :] with P_h (bf16 pairs) at columns [64h, 64h+32)
+      const uint64_t q_desc = make_desc_sw128(sQ, 16, 1024);
+      const uint64_t k_desc0 = make_desc_sw128(sK, 16, 1024);
+      const uint64_t v_desc0 = make_desc_sw128(sV, kHalfBytes, 1024);
+      const int me = (warp == 1) ? 0 : 1;
+      bool ok = true;
+      if (me == 0) {
+        ok = wd.wait(&bars.q_full, 0);
+        for (int t = 0; ok && t < n_kv; ++t) {
+          const int ks_st = t % kStages;
+          if (!(ok = wd.wait(&bars.k_full[ks_st], (t / kStages) & 1))) break;
+          if (t >= 2 && !(ok = wd.wait(&bars.pv_done[t & 1], ((t - 2) >> 1) & 1))) break;
+          tc_fence_after_sync();
+          const uint64_t kd = k_desc0 + static_cast<uint64_t>(ks_st * kTileUnits);
 #pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks)
-          umma_bf16_ts(tmem + kColO + (ks >> 2) * 128, pa + (ks >> 2) * 64 + (ks & 3) * 8,
-                       v_mn_desc(va, ks), idesc_o, (u > 0 || (ks & 3) > 0) ? 1u : 0u);
-        umma_commit(&bars.pv_done[u & 1]);
-        umma_commit(&bars.v_empty[vs]);
-        return true;
-      };
-      for (int t = 0; ok && t < n_kv; ++t) {
-        const int ks_st = t % kStages;
-        if (!(ok = wd.wait(&bars.k_full[ks_st], (t / kStages) & 1))) break;
-        tc_fence_after_sync();
-        const uint32_t ka = sK + ks_st * kTileBytes;
-        // S(t) overwrites P(t-2) in buffer t&1: PV(t-2) was issued earlier and
-        // tcgen05 MMAs of one thread execute in issue order
+          for (int ks = 0; ks < kD / 16; ++ks)
+            umma_bf16_ss(tmem + kColS + (t & 1) * kBN, q_desc + kmajor_off(ks), kd + kmajor_off(ks), idesc_s,
+                         ks > 0 ? 1u : 0u);
+          umma_commit(&bars.s_full[t & 1]);
+          umma_commit(&bars.k_empty[ks_st]);
+        }
+      } else {
+        for (int u = 0; ok && u < n_kv; ++u) {
+          const int vs = u % kStages;
+          if (!(ok = wd.wait(&bars.v_full[vs], (u / kStages) & 1))) break;
+          if (!(ok = wd.wait(&bars.p_full[u & 1], (u >> 1) & 1))) break;
+          tc_fence_after_sync();
+          const uint64_t vd = v_desc0 + static_cast<uint64_t>(vs * kTileUnits);
+          const uint32_t pa = tmem + kColS + (u & 1) * kBN;   // P in the S buffer, lane 0
+          // O_h += P_h V[64h:64h+64, :] with P_h (bf16 pairs) at columns
+          // [64h, 64h+32); the two halves' chains interleaved
 #pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks)
-          umma_bf16_ss(tmem + kColS + (t & 1) * kBN, kmajor_desc(sQ, ks), kmajor_desc(ka, ks), idesc_s,
-                       ks > 0 ? 1u : 0u);
-        umma_commit(&bars.s_full[t & 1]);
-        umma_commit(&bars.k_empty[ks_st]);
-        if (t >= 1) ok = issue_pv(t - 1);
+          for (int j = 0; j < kBN / 16; ++j) {
+            const int ks = (j >> 1) + 4 * (j & 1);
+            umma_bf16_ts(tmem + kColO + (ks >> 2) * 128, pa + (ks >> 2) * 64 + (ks & 3) * 8,
+                         vd + vmn_off(ks), idesc_o, (u > 0 || (ks & 3) > 0) ? 1u : 0u);
+          }
+          umma_commit(&bars.pv_done[u & 1]);
+          umma_commit(&bars.v_empty[vs]);
+        }
       }
-      if (ok) issue_pv(n_kv - 1);
       // every MMA this thread issued has completed before TMEM is released
-      umma_commit(&bars.mma_final);
-      wd.drain(&bars.mma_final, 0, 4000000);
+      umma_commit(&bars.mma_final[me]);
+      wd.drain(&bars.mma_final[me], 0, 4000000);
     }
   } else {
     // ------------------------------------------------------------ softmax
