@@ -11,24 +11,30 @@
 //
 // One CTA owns one 128-key tile of one key/value head: it loops over the G
 // query heads of the group and the chunk's 64-row query tiles that can see the
-// tile, keeps dK and dV for its 128 keys in TMEM for the whole loop, and
-// finally adds them into the float32 accumulators with a plain
+// tile ("steps"), keeps dK and dV for its 128 keys in TMEM for the whole loop,
+// and finally adds them into the float32 accumulators with a plain
 // read-modify-write (no other CTA touches those rows in this call, so there is
 // no atomic contention across query tiles).  dQ partial products of every key
 // tile are summed into the zeroed dq with fp32 reductions.
+//
+// TMEM (512 columns): dK [0,128), dV [128,256) and two step buffers of 128
+// columns.  Step n uses buffer n&1: S^T in its first 64 columns, dP^T in the
+// last 64.  The compute warps read S^T/dP^T and write P^T/dS^T (bf16 pairs)
+// back over them; the dK MMA reads dS^T there, and dQ^T then overwrites the
+// dP^T half.  Two buffers let the S^T/dP^T MMAs of step n+1 run while the
+// compute warps form P and dS of step n.
 //   warp 0       TMA producer: K, V once; Q, dO (64 rows) + L, Delta per step
-//                into a 3-stage ring (the load for step n+3 is issued when
-//                step n's MMAs finish, so its latency hides behind two steps)
-//   warp 1       TMEM owner + MMA issuer (one thread):
-//                  S^T = K Q^T, dP^T = V dO^T  (M=128 keys, N=64, K=128; SS)
-//                  dV += P^T dO, dK += dS^T Q  (M=128 keys, N=128, K=64; A in TMEM)
-//                  dQ^T = K^T dS^T             (M=128 d, N=64, K=128; SS)
-//   warps 2..9   P^T, dS^T: two warps per TMEM lane quadrant, 32 query columns
-//                each; P^T/dS^T (bf16) go to TMEM for dV/dK and dS^T also to
-//                shared memory for dQ; the final dK (warps 2-5) / dV (6-9) RMW
+//                into a 3-stage ring
+//   warp 1       TMEM owner + MMA issuer A: S^T = K Q^T, dP^T = V dO^T
+//                (M=128 keys, N=64, K=128; SS), up to two steps ahead
+//   warp 14      MMA issuer B: dV += P^T dO, dK += dS^T Q (M=128, N=128, K=64;
+//                A from TMEM), dQ^T = K^T dS^T (M=128 d, N=64, K=128; SS)
+//   warps 2..9   P^T, dS^T: two warps per TMEM lane quadrant, 32 query
+//                columns each; dS^T also to shared memory for dQ^T; the final
+//                dK (warps 2-5) / dV (6-9) read-modify-write
 //   warps 10..13 dQ^T from TMEM -> fp32 reductions into dq
-// The next step's S^T/dP^T MMAs are issued before this step's dV/dK/dQ MMAs,
-// so the tensor pipe works while the compute warps form P and dS.
+// Two issuing threads because one thread keeps only about one tcgen05.mma in
+// flight per ~90 cycles.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -42,7 +48,8 @@ constexpr int kBQ = 64;    // query rows per step
 constexpr int kD = 128;    // head dim
 constexpr int kComputeWarps = 8;                      // two per TMEM lane quadrant
 constexpr int kDQWarp0 = 2 + kComputeWarps;            // 4 dQ warps
-constexpr int kThreads = 32 * (kDQWarp0 + 4);         // 14 warps
+constexpr int kIssuerB = kDQWarp0 + 4;                 // second MMA issuer
+constexpr int kThreads = 32 * (kIssuerB + 1);          // 15 warps
 
 constexpr int kKVTileBytes = kBK * kD * 2;         // 32 KB
 constexpr int kKVHalf = kKVTileBytes / 2;          // 16 KB: 128 rows x 128 B
@@ -51,9 +58,9 @@ constexpr int kQHalf = kQTileBytes / 2;            // 8 KB: 64 rows x 128 B
 constexpr int kPTileBytes = kBK * kBQ * 2;         // 16 KB: 128 keys x 64 q
 
 // shared memory carve-up (bytes from the 1024-aligned base)
+constexpr int kQStages = 3;                              // Q/dO/L/Delta ring depth
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kKVTileBytes;
-constexpr int kQStages = 3;                              // Q/dO/L/Delta ring depth
 constexpr int kOffQ = kOffV + kKVTileBytes;              // kQStages stages
 constexpr int kOffDO = kOffQ + kQStages * kQTileBytes;   // kQStages stages
 constexpr int kOffDS = kOffDO + kQStages * kQTileBytes;  // 2 buffers
@@ -65,11 +72,9 @@ constexpr int kSmemAlloc = kSmemBytes + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColDK = 0;
 constexpr uint32_t kColDV = 128;
-constexpr uint32_t kColS = 256;
-constexpr uint32_t kColDP = 320;
-constexpr uint32_t kColDQ = 384;
-constexpr uint32_t kColPT = 448;   // P^T as bf16 pairs (32 columns), A operand of dV
-constexpr uint32_t kColDST = 480;  // dS^T as bf16 pairs (32 columns), A operand of dK
+__host__ __device__ constexpr uint32_t col_buf(int b) { return 256u + 128u * static_cast<uint32_t>(b); }
+constexpr uint32_t kOffS = 0;    // within a step buffer: S^T, then P^T pairs at [32h, 32h+16)
+constexpr uint32_t kOffDP = 64;  // dP^T, then dS^T pairs at [32h, 32h+16), then dQ^T (64 cols)
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -91,12 +96,13 @@ struct BwdParams {
 struct BwdBarriers {
   uint64_t kv_full;
   uint64_t q_full[kQStages], q_empty[kQStages];
-  uint64_t sdp_full;
-  uint64_t ds_full[2], ds_empty[2];
-  uint64_t dq_full, dq_empty;
-  uint64_t pds_free;  // dV/dK MMAs of a step done: P^T/dS^T columns reusable
+  uint64_t sdp_full[2];    // S^T/dP^T of buffer b computed (issuer A)
+  uint64_t ds_full[2];     // P^T/dS^T of buffer b written (compute warps)
+  uint64_t ds_empty[2];    // dS^T shared-memory buffer b read by dQ^T (issuer B)
+  uint64_t dq_full[2];     // dQ^T in buffer b computed (issuer B)
+  uint64_t dq_empty[2];    // dQ^T of buffer b drained (dQ warps)
   uint64_t acc_done;
-  uint64_t mma_final;
+  uint64_t mma_final[2];
 };
 
 __device__ __forceinline__ bool warp_wait(Watchdog& wd, uint64_t* bar, uint32_t parity) {
@@ -104,16 +110,22 @@ __device__ __forceinline__ bool warp_wait(Watchdog& wd, uint64_t* bar, uint32_t 
   return __all_sync(0xffffffffu, ok);
 }
 
-// K-major operand whose rows are `rows` long blocks of 128 B (64 bf16 of K):
-// K-step ks (16 elements) lies in block ks/4 at byte 32*(ks%4) of each row.
-__device__ __forceinline__ uint64_t kmajor(uint32_t base, int block_bytes, int ks) {
-  return make_desc_sw128(base + (ks >> 2) * block_bytes + (ks & 3) * 32, 16, 1024);
+// Shared-memory descriptors are built once per tile base; a K-step moves only
+// the 14-bit start-address field (16-byte units), so each MMA's operands are
+// the base plus a compile-time constant.
+// K-major operand stored as 128-byte rows in blocks of `block_bytes` (64 bf16
+// of K per block): K-step ks (16 elements) lies in block ks/4 at byte
+// 32*(ks%4) of each row.
+__host__ __device__ constexpr uint32_t kmajor_off(int block_bytes, int ks) {
+  return static_cast<uint32_t>(((ks >> 2) * block_bytes + (ks & 3) * 32) >> 4);
 }
 // MN-major operand stored as [K rows][MN] with 128-byte rows: 8 K-rows per
-// 1024-byte atom, `mn_block_bytes` between 64-wide MN blocks; K-step ks
-// (16 rows) starts 2048 bytes further.
-__device__ __forceinline__ uint64_t mnmajor(uint32_t base, int mn_block_bytes, int ks) {
-  return make_desc_sw128(base + ks * 2048, mn_block_bytes, 1024);
+// 1024-byte atom; K-step ks (16 rows) starts 2048 bytes further.
+__host__ __device__ constexpr uint32_t mnmajor_off(int ks) { return static_cast<uint32_t>((ks * 2048) >> 4); }
+// Column (relative to a step buffer's half) of the bf16 pairs of query rows
+// [16 ks, 16 ks + 16): compute warp half h packs its 32 rows at [32h, 32h+16).
+__host__ __device__ constexpr uint32_t pair_col(int ks) {
+  return static_cast<uint32_t>(32 * (ks >> 1) + 8 * (ks & 1));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -151,18 +163,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars.kv_full, 1);
     for (int i = 0; i < kQStages; ++i) {
       mbar_init(&bars.q_full[i], 1);
-      mbar_init(&bars.q_empty[i], 1);
+      mbar_init(&bars.q_empty[i], 2);   // one commit from each MMA issuer
     }
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.sdp_full[i], 1);
       mbar_init(&bars.ds_full[i], kComputeWarps * 32);
       mbar_init(&bars.ds_empty[i], 1);
+      mbar_init(&bars.dq_full[i], 1);
+      mbar_init(&bars.dq_empty[i], 4 * 32);
+      mbar_init(&bars.mma_final[i], 1);
     }
-    mbar_init(&bars.sdp_full, 1);
-    mbar_init(&bars.dq_full, 1);
-    mbar_init(&bars.dq_empty, 4 * 32);
     mbar_init(&bars.acc_done, 1);
-    mbar_init(&bars.pds_free, 1);
-    mbar_init(&bars.mma_final, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -220,69 +231,79 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (issued[st] > 0) wd.drain(&bars.q_full[st], ((issued[st] - 1) / kQStages) & 1, 1000000);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kIssuerB) {
+    // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
       const uint32_t idesc_sdp = make_idesc_bf16(kBK, kBQ, false, false);  // M128 N64, K-major both
       const uint32_t idesc_kv = make_idesc_bf16(kBK, kD, false, true);     // M128 N128, B MN-major
       const uint32_t idesc_dq = make_idesc_bf16(kD, kBQ, true, true);      // M128 N64, both MN-major
-      auto issue_sdp = [&](int n) -> bool {
-        const int st = n % kQStages;
-        if (!wd.wait(&bars.q_full[st], (n / kQStages) & 1)) return false;
-        tc_fence_after_sync();
-        const uint32_t qa = sQ + st * kQTileBytes;
-        const uint32_t da = sDO + st * kQTileBytes;
+      const bool is_a = (warp == 1);
+      bool ok = true;
+      if (is_a) {
+        // ---- issuer A: S^T(n) and dP^T(n) into buffer n&1, as early as the
+        // Q/dO stage has landed and step n-2 has released the buffer
+        const uint64_t k_kmaj = make_desc_sw128(sK, 16, 1024);
+        const uint64_t v_kmaj = make_desc_sw128(sV, 16, 1024);
+        const uint64_t q_kmaj0 = make_desc_sw128(sQ, 16, 1024);
+        const uint64_t do_kmaj0 = make_desc_sw128(sDO, 16, 1024);
+        ok = wd.wait(&bars.kv_full, 0);
+        for (int n = 0; ok && n < n_steps; ++n) {
+          const int st = n % kQStages;
+          const int bb = n & 1;
+          if (!(ok = wd.wait(&bars.q_full[st], (n / kQStages) & 1))) break;
+          if (n >= 2 && !(ok = wd.wait(&bars.dq_empty[bb], ((n - 2) >> 1) & 1))) break;
+          tc_fence_after_sync();
+          const uint64_t qd = q_kmaj0 + static_cast<uint64_t>(st * (kQTileBytes >> 4));
+          const uint64_t dd = do_kmaj0 + static_cast<uint64_t>(st * (kQTileBytes >> 4));
+          const uint32_t cb = tmem + col_buf(bb);
 #pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks)
-          umma_bf16_ss(tmem + kColS, kmajor(sK, kKVHalf, ks), kmajor(qa, kQHalf, ks), idesc_sdp,
-                       ks > 0 ? 1u : 0u);
+          for (int ks = 0; ks < kD / 16; ++ks) {
+            umma_bf16_ss(cb + kOffS, k_kmaj + kmajor_off(kKVHalf, ks), qd + kmajor_off(kQHalf, ks), idesc_sdp,
+                         ks > 0 ? 1u : 0u);
+            umma_bf16_ss(cb + kOffDP, v_kmaj + kmajor_off(kKVHalf, ks), dd + kmajor_off(kQHalf, ks), idesc_sdp,
+                         ks > 0 ? 1u : 0u);
+          }
+          umma_commit(&bars.sdp_full[bb]);
+          umma_commit(&bars.q_empty[st]);   // issuer A's readers of the stage are done
+        }
+        umma_commit(&bars.mma_final[0]);
+        wd.drain(&bars.mma_final[0], 0, 4000000);
+      } else {
+        // ---- issuer B: dV, dK, then dQ^T of step n once P^T/dS^T are written
+        const uint64_t k_mn = make_desc_sw128(sK, kKVHalf, 1024);
+        const uint64_t q_mn0 = make_desc_sw128(sQ, kQHalf, 1024);
+        const uint64_t do_mn0 = make_desc_sw128(sDO, kQHalf, 1024);
+        const uint64_t ds_mn0 = make_desc_sw128(sDS, kPTileBytes, 1024);
+        for (int n = 0; ok && n < n_steps; ++n) {
+          const int st = n % kQStages;
+          const int bb = n & 1;
+          if (!(ok = wd.wait(&bars.ds_full[bb], (n >> 1) & 1))) break;
+          tc_fence_after_sync();
+          const uint64_t qm = q_mn0 + static_cast<uint64_t>(st * (kQTileBytes >> 4));
+          const uint64_t dm = do_mn0 + static_cast<uint64_t>(st * (kQTileBytes >> 4));
+          const uint64_t sm = ds_mn0 + static_cast<uint64_t>(bb * (kPTileBytes >> 4));
+          const uint32_t cb = tmem + col_buf(bb);
+          // dV += P^T dO ; dK += dS^T Q  (K = 64 query rows: 4 steps), interleaved
 #pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks)
-          umma_bf16_ss(tmem + kColDP, kmajor(sV, kKVHalf, ks), kmajor(da, kQHalf, ks), idesc_sdp,
-                       ks > 0 ? 1u : 0u);
-        umma_commit(&bars.sdp_full);
-        return true;
-      };
-      auto issue_grads = [&](int n) -> bool {
-        const int st = n % kQStages;
-        const int db = n & 1;
-        const uint32_t qa = sQ + st * kQTileBytes;
-        const uint32_t da = sDO + st * kQTileBytes;
-        const uint32_t dsa = sDS + db * kPTileBytes;
-        // dV += P^T dO ; dK += dS^T Q   (A from TMEM; K = 64 query rows: 4 steps)
+          for (int ks = 0; ks < kBQ / 16; ++ks) {
+            umma_bf16_ts(tmem + kColDV, cb + kOffS + pair_col(ks), dm + mnmajor_off(ks), idesc_kv,
+                         (n > 0 || ks > 0) ? 1u : 0u);
+            umma_bf16_ts(tmem + kColDK, cb + kOffDP + pair_col(ks), qm + mnmajor_off(ks), idesc_kv,
+                         (n > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(&bars.q_empty[st]);   // issuer B's readers of the stage are done
+          // dQ^T = K^T dS^T (K = 128 keys) over the dP^T half: issued after dK,
+          // which read dS^T there (one thread's MMAs run in issue order)
 #pragma unroll
-        for (int ks = 0; ks < kBQ / 16; ++ks)
-          umma_bf16_ts(tmem + kColDV, tmem + kColPT + ks * 8, mnmajor(da, kQHalf, ks), idesc_kv,
-                       (n > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < kBQ / 16; ++ks)
-          umma_bf16_ts(tmem + kColDK, tmem + kColDST + ks * 8, mnmajor(qa, kQHalf, ks), idesc_kv,
-                       (n > 0 || ks > 0) ? 1u : 0u);
-        umma_commit(&bars.pds_free);
-        // dQ^T = K^T dS^T  (K = 128 keys: 8 steps); the dQ warps must have
-        // drained the previous step's dQ^T
-        if (n >= 1 && !wd.wait(&bars.dq_empty, (n - 1) & 1)) return false;
-        tc_fence_after_sync();
-#pragma unroll
-        for (int ks = 0; ks < kBK / 16; ++ks)
-          umma_bf16_ss(tmem + kColDQ, mnmajor(sK, kKVHalf, ks), mnmajor(dsa, kPTileBytes, ks), idesc_dq,
-                       ks > 0 ? 1u : 0u);
-        umma_commit(&bars.dq_full);
-        umma_commit(&bars.q_empty[st]);
-        umma_commit(&bars.ds_empty[db]);
-        return true;
-      };
-      bool ok = wd.wait(&bars.kv_full, 0);
-      if (ok && n_steps > 0) ok = issue_sdp(0);
-      for (int n = 0; ok && n < n_steps; ++n) {
-        if (!(ok = wd.wait(&bars.ds_full[n & 1], (n >> 1) & 1))) break;
-        tc_fence_after_sync();
-        if (n + 1 < n_steps && !(ok = issue_sdp(n + 1))) break;
-        ok = issue_grads(n);
+          for (int ks = 0; ks < kBK / 16; ++ks)
+            umma_bf16_ss(cb + kOffDP, k_mn + mnmajor_off(ks), sm + mnmajor_off(ks), idesc_dq, ks > 0 ? 1u : 0u);
+          umma_commit(&bars.dq_full[bb]);
+          umma_commit(&bars.ds_empty[bb]);
+        }
+        umma_commit(&bars.acc_done);
+        umma_commit(&bars.mma_final[1]);
+        wd.drain(&bars.mma_final[1], 0, 4000000);
       }
-      umma_commit(&bars.acc_done);
-      umma_commit(&bars.mma_final);
-      wd.drain(&bars.mma_final, 0, 4000000);
     }
   } else if (warp < 2 + kComputeWarps) {
     // ------------------------------------------------------------ P / dS
@@ -297,15 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int n = 0; n < n_steps; ++n) {
       const int st = n % kQStages;
-      const int db = n & 1;
+      const int bb = n & 1;
       const int qi = step_qtile(n);
-      if (!(ok = warp_wait(wd, &bars.sdp_full, n & 1))) break;
+      // the L/Delta statistics of the stage first: they load while S^T/dP^T compute
       if (!(ok = warp_wait(wd, &bars.q_full[st], (n / kQStages) & 1))) break;
-      if (n >= 2 && !(ok = warp_wait(wd, &bars.ds_empty[db], ((n - 2) >> 1) & 1))) break;
-      tc_fence_after_sync();
-      uint32_t rs[32], rp[32];
-      tmem_ld32(tmem + lane_base + kColS + c_off, rs);
-      tmem_ld32(tmem + lane_base + kColDP + c_off, rp);
       const float4* L4 = reinterpret_cast<const float4*>(stat + st * 2 * kBQ + c_off);
       const float4* D4 = reinterpret_cast<const float4*>(stat + st * 2 * kBQ + kBQ + c_off);
       float lse2[32], dl[32];
@@ -316,6 +332,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         lse2[4 * j + 2] = -l.z * kLog2e; lse2[4 * j + 3] = -l.w * kLog2e;
         dl[4 * j] = dd.x; dl[4 * j + 1] = dd.y; dl[4 * j + 2] = dd.z; dl[4 * j + 3] = dd.w;
       }
+      if (!(ok = warp_wait(wd, &bars.sdp_full[bb], (n >> 1) & 1))) break;
+      tc_fence_after_sync();
+      const uint32_t cb = tmem + lane_base + col_buf(bb);
+      uint32_t rs[32], rp[32];
+      tmem_ld32(cb + kOffS + c_off, rs);
+      tmem_ld32(cb + kOffDP + c_off, rp);
       const bool masked = diag_tile && (qi - qi_first) < 2;
       const int q_abs0 = p.q_start + qi * kBQ + c_off;  // absolute row of this warp's column 0
       tmem_ld_wait();
@@ -332,24 +354,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk[j / 2] = pack_bf16x2(p0 * (__uint_as_float(rp[j]) - dl[j]),
                                 p1 * (__uint_as_float(rp[j + 1]) - dl[j + 1]));
       }
-      // dS^T row segment to shared memory (B operand of dQ^T): 128-byte rows,
-      // 128-byte swizzle inside 8-row groups; this warp writes 16-byte chunks
-      // 4*half .. 4*half+3 of its rows
+      // P^T/dS^T pairs back over this warp's own S^T/dP^T columns
+      tmem_st16(cb + kOffS + c_off, pp);
+      tmem_st16(cb + kOffDP + c_off, pk);
+      // dS^T row segment to shared memory (B operand of dQ^T) once dQ^T of
+      // step n-2 has read that buffer: 128-byte rows, 128-byte swizzle inside
+      // 8-row groups; this warp writes 16-byte chunks 4*half .. 4*half+3
+      if (n >= 2 && !(ok = warp_wait(wd, &bars.ds_empty[bb], ((n - 2) >> 1) & 1))) break;
       const uint32_t sw = static_cast<uint32_t>(kr & 7);
-      const uint32_t dsrow = sDS + db * kPTileBytes + kr * 128;
+      const uint32_t dsrow = sDS + bb * kPTileBytes + kr * 128;
 #pragma unroll
       for (int ci = 0; ci < 4; ++ci)
         st_shared_v4(dsrow + (((4 * half + ci) ^ sw) << 4), pk[ci * 4], pk[ci * 4 + 1], pk[ci * 4 + 2],
                      pk[ci * 4 + 3]);
-      // P^T and dS^T segments to TMEM (A operands of dV and dK) once the
-      // previous step's dV/dK MMAs have read the old ones
-      if (n >= 1 && !(ok = warp_wait(wd, &bars.pds_free, (n - 1) & 1))) break;
-      tmem_st16(tmem + lane_base + kColPT + 16 * half, pp);
-      tmem_st16(tmem + lane_base + kColDST + 16 * half, pk);
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before_sync();
-      mbar_arrive(&bars.ds_full[db]);
+      mbar_arrive(&bars.ds_full[bb]);
     }
     // ---- epilogue: this tile's dK (half 0) or dV (half 1) rows into the running sums
     if (ok) ok = warp_wait(wd, &bars.acc_done, 0);
@@ -391,14 +412,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int dcol = quad * 32 + lane;                  // head-dim column (TMEM lane)
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     for (int n = 0; n < n_steps; ++n) {
-      if (!warp_wait(wd, &bars.dq_full, n & 1)) break;
+      const int bb = n & 1;
+      if (!warp_wait(wd, &bars.dq_full[bb], (n >> 1) & 1)) break;
       tc_fence_after_sync();
       uint32_t r0[32], r1[32];
-      tmem_ld32(tmem + lane_base + kColDQ, r0);
-      tmem_ld32(tmem + lane_base + kColDQ + 32, r1);
+      tmem_ld32(tmem + lane_base + col_buf(bb) + kOffDP, r0);
+      tmem_ld32(tmem + lane_base + col_buf(bb) + kOffDP + 32, r1);
       tmem_ld_wait();
       tc_fence_before_sync();
-      mbar_arrive(&bars.dq_empty);
+      mbar_arrive(&bars.dq_empty[bb]);
       const int h = step_head(n);
       const int qi = step_qtile(n);
       float* base = p.dq + ((static_cast<int64_t>(b) * p.q_len + qi * kBQ) * p.Hq + h) * kD + dcol;
