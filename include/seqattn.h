@@ -84,8 +84,8 @@ typedef struct {
  *     q_len == 0 is a no-op.
  *   softmax_scale: finite, > 0 (usually 1/sqrt(d)).
  *   o (out), lse (out): overwritten.
- * BF16 requires d == 128 and q_start, q_len, prefix_len multiples of 128
- * (else SEQATTN_ERR_UNSUPPORTED).  FP32 accepts any sizes and d in {64, 128}.
+ * BF16 requires d == 128 (else SEQATTN_ERR_UNSUPPORTED) and accepts any
+ * q_start, q_len, prefix_len.  FP32 accepts any sizes and d in {64, 128}.
  */
 seqattn_status seqattn_chunk_fwd(const seqattn_problem* pb, int64_t q_start, int64_t q_len,
                                  int64_t prefix_len, float softmax_scale, const void* q,
@@ -125,10 +125,11 @@ seqattn_status seqattn_chunk_bwd(const seqattn_problem* pb, int64_t q_start, int
  * exactly what seqattn_chunk_bwd computes, with the same arguments minus the
  * workspace, and calls no allocation routine.
  *
- * Its scratch (Delta, B * Hq * q_len floats) is a fixed device array inside
- * the library of SEQATTN_NOALLOC_MAX_DELTA floats (4 MiB), which every GPU
- * that loads the library holds until the process exits.  Larger requests
- * return SEQATTN_ERR_INVALID_ARG (use seqattn_chunk_bwd instead).  The first
+ * Its scratch (the per-row statistics, seqattn_bwd_workspace_size(pb, q_len)
+ * bytes) is a fixed device array inside the library of
+ * SEQATTN_NOALLOC_MAX_DELTA floats (4 MiB), which every GPU that loads the
+ * library holds until the process exits.  Larger requests return
+ * SEQATTN_ERR_INVALID_ARG (use seqattn_chunk_bwd instead).  The first
  * call on a device looks up that device's address of the array; make that
  * first call before any stream capture.  Every call shares the one array, so
  * calls that overlap on the GPU (different streams, or different host

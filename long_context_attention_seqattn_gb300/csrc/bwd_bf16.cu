@@ -15,26 +15,32 @@
 // and finally adds them into the float32 accumulators with a plain
 // read-modify-write (no other CTA touches those rows in this call, so there is
 // no atomic contention across query tiles).  dQ partial products of every key
-// tile are summed into the zeroed dq with fp32 reductions.
+// tile are summed into the zeroed dq with fp32 reductions.  Chunks may start
+// and end anywhere: a partial last query tile reads padding statistics
+// (-inf, 0) that make its extra rows' P exactly 0, and rows past the chunk
+// are never stored.
 //
 // TMEM (512 columns): dK [0,128), dV [128,256) and two step buffers of 128
 // columns.  Step n uses buffer n&1: S^T in its first 64 columns, dP^T in the
-// last 64.  The compute warps read S^T/dP^T and write P^T/dS^T (bf16 pairs)
-// back over them; the dK MMA reads dS^T there, and dQ^T then overwrites the
-// dP^T half.  Two buffers let the S^T/dP^T MMAs of step n+1 run while the
-// compute warps form P and dS of step n.
-//   warp 0       TMA producer: K, V once; Q, dO (64 rows) + L, Delta per step
-//                into a 3-stage ring
-//   warp 1       TMEM owner + MMA issuer A: S^T = K Q^T, dP^T = V dO^T
-//                (M=128 keys, N=64, K=128; SS), up to two steps ahead
-//   warp 14      MMA issuer B: dV += P^T dO, dK += dS^T Q (M=128, N=128, K=64;
-//                A from TMEM), dQ^T = K^T dS^T (M=128 d, N=64, K=128; SS)
-//   warps 2..9   P^T, dS^T: two warps per TMEM lane quadrant, 32 query
+// last 64.  Compute warp half h reads S^T columns [32h, 32h+32) and writes P^T
+// (bf16 pairs) over the first 16 of them and dS^T over the last 16, so the dP^T
+// half is free as soon as it has been read and dQ^T can land there.  Two
+// buffers let the S^T/dP^T MMAs of step n+1 run while the compute warps form P
+// and dS of step n.
+//   warp 0       TMA producer: K, V once; Q, dO (64 rows) + the step's row
+//                statistics (-L log2 e, Delta) into a 3-stage ring
+//   warp 1       TMEM owner + MMA issuer of S^T = K Q^T (M=128 keys, N=64, SS)
+//   warp 15      MMA issuer of dP^T = V dO^T (M=128 keys, N=64, SS)
+//   warp 14      MMA issuer of dV += P^T dO (as soon as P^T is written),
+//                dK += dS^T Q (M=128, N=128, K=64; A from TMEM) and
+//                dQ^T = K^T dS^T (M=128 d, N=64, K=128; SS)
+//   warps 2..9   P^T, then dS^T: two warps per TMEM lane quadrant, 32 query
 //                columns each; dS^T also to shared memory for dQ^T; the final
 //                dK (warps 2-5) / dV (6-9) read-modify-write
 //   warps 10..13 dQ^T from TMEM -> fp32 reductions into dq
-// Two issuing threads because one thread keeps only about one tcgen05.mma in
-// flight per ~90 cycles.
+// Three issuing threads because one thread keeps only about one tcgen05.mma
+// in flight per ~90 cycles, whatever its shape; S^T and dP^T, which gate the
+// compute warps, each get a thread of their own.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -48,8 +54,9 @@ constexpr int kBQ = 64;    // query rows per step
 constexpr int kD = 128;    // head dim
 constexpr int kComputeWarps = 8;                      // two per TMEM lane quadrant
 constexpr int kDQWarp0 = 2 + kComputeWarps;            // 4 dQ warps
-constexpr int kIssuerB = kDQWarp0 + 4;                 // second MMA issuer
-constexpr int kThreads = 32 * (kIssuerB + 1);          // 15 warps
+constexpr int kIssuerKV = kDQWarp0 + 4;                // dV, dK, dQ^T issuer
+constexpr int kIssuerDP = kIssuerKV + 1;               // dP^T issuer
+constexpr int kThreads = 32 * (kIssuerDP + 1);          // 16 warps
 
 constexpr int kKVTileBytes = kBK * kD * 2;         // 32 KB
 constexpr int kKVHalf = kKVTileBytes / 2;          // 16 KB: 128 rows x 128 B
@@ -58,13 +65,13 @@ constexpr int kQHalf = kQTileBytes / 2;            // 8 KB: 64 rows x 128 B
 constexpr int kPTileBytes = kBK * kBQ * 2;         // 16 KB: 128 keys x 64 q
 
 // shared memory carve-up (bytes from the 1024-aligned base)
-constexpr int kQStages = 3;                              // Q/dO/L/Delta ring depth
+constexpr int kQStages = 3;                              // Q/dO/statistics ring depth
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kKVTileBytes;
 constexpr int kOffQ = kOffV + kKVTileBytes;              // kQStages stages
 constexpr int kOffDO = kOffQ + kQStages * kQTileBytes;   // kQStages stages
 constexpr int kOffDS = kOffDO + kQStages * kQTileBytes;  // 2 buffers
-constexpr int kOffStat = kOffDS + 2 * kPTileBytes;       // kQStages x (L[64], Delta[64])
+constexpr int kOffStat = kOffDS + 2 * kPTileBytes;       // kQStages x (-L log2 e [64], Delta [64])
 constexpr int kStatBytes = 2 * kBQ * 4;
 constexpr int kSmemBytes = kOffStat + kQStages * kStatBytes;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
@@ -73,20 +80,18 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColDK = 0;
 constexpr uint32_t kColDV = 128;
 __host__ __device__ constexpr uint32_t col_buf(int b) { return 256u + 128u * static_cast<uint32_t>(b); }
-constexpr uint32_t kOffS = 0;    // within a step buffer: S^T, then P^T pairs at [32h, 32h+16)
-constexpr uint32_t kOffDP = 64;  // dP^T, then dS^T pairs at [32h, 32h+16), then dQ^T (64 cols)
-
-constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kOffS = 0;    // within a step buffer: S^T, then P^T / dS^T pairs
+constexpr uint32_t kOffDP = 64;  // dP^T, then dQ^T (64 cols)
 
 struct BwdParams {
   int B, Hq, Hkv, G;
   int q_len, T;
   int q_start, kv_begin;
   int n_ktiles;
+  int n_q64;               // 64-row query tiles of the chunk (the last may be partial)
   float scale;
   float scale_log2;
-  const float* lse;
-  const float* delta;
+  const float* stats;      // [B, Hq, n_q64, 2, 64]: -L log2 e, then Delta, per query tile
   float* dq;
   float* dk;
   float* dv;
@@ -96,13 +101,16 @@ struct BwdParams {
 struct BwdBarriers {
   uint64_t kv_full;
   uint64_t q_full[kQStages], q_empty[kQStages];
-  uint64_t sdp_full[2];    // S^T/dP^T of buffer b computed (issuer A)
-  uint64_t ds_full[2];     // P^T/dS^T of buffer b written (compute warps)
-  uint64_t ds_empty[2];    // dS^T shared-memory buffer b read by dQ^T (issuer B)
-  uint64_t dq_full[2];     // dQ^T in buffer b computed (issuer B)
+  uint64_t s_full[2];      // S^T of buffer b computed
+  uint64_t dp_full[2];     // dP^T of buffer b computed
+  uint64_t p_full[2];      // P^T of buffer b written (compute warps)
+  uint64_t ds_full[2];     // dS^T of buffer b written to TMEM and smem (compute warps)
+  uint64_t kv_done[2];     // dV, dK of buffer b done: the S^T half is free
+  uint64_t ds_empty[2];    // dS^T shared-memory buffer b read by dQ^T
+  uint64_t dq_full[2];     // dQ^T in buffer b computed
   uint64_t dq_empty[2];    // dQ^T of buffer b drained (dQ warps)
   uint64_t acc_done;
-  uint64_t mma_final[2];
+  uint64_t mma_final[3];
 };
 
 __device__ __forceinline__ bool warp_wait(Watchdog& wd, uint64_t* bar, uint32_t parity) {
@@ -122,11 +130,13 @@ __host__ __device__ constexpr uint32_t kmajor_off(int block_bytes, int ks) {
 // MN-major operand stored as [K rows][MN] with 128-byte rows: 8 K-rows per
 // 1024-byte atom; K-step ks (16 rows) starts 2048 bytes further.
 __host__ __device__ constexpr uint32_t mnmajor_off(int ks) { return static_cast<uint32_t>((ks * 2048) >> 4); }
-// Column (relative to a step buffer's half) of the bf16 pairs of query rows
-// [16 ks, 16 ks + 16): compute warp half h packs its 32 rows at [32h, 32h+16).
+// Column (relative to a step buffer) of the P^T bf16 pairs of query rows
+// [16 ks, 16 ks + 16): compute warp half h packs its 32 rows at [32h, 32h+16);
+// the dS^T pairs of the same rows sit 16 columns further.
 __host__ __device__ constexpr uint32_t pair_col(int ks) {
   return static_cast<uint32_t>(32 * (ks >> 1) + 8 * (ks & 1));
 }
+constexpr uint32_t kDSPairs = 16;
 
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_bf16_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -148,12 +158,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = idx % p.Hkv;
   const int b = idx / p.Hkv;
   const int kb = p.kv_begin + kt * kBK;                  // absolute first key of the tile
-  const int n_q64 = p.q_len / kBQ;
-  // first query tile that sees any key of this tile; the two tiles covering
-  // the diagonal 128 block carry the causal mask
-  const int qi_first = kb >= p.q_start ? (kb - p.q_start) / kBQ : 0;
-  const bool diag_tile = kb >= p.q_start;
-  const int nq = n_q64 - qi_first;
+  const int q_end = p.q_start + p.q_len;                 // one past the chunk's last row
+  // first query tile that sees any key of this tile (the one holding row kb)
+  const int qi_first = kb > p.q_start ? (kb - p.q_start) / kBQ : 0;
+  const int nq = p.n_q64 - qi_first;
   const int n_steps = p.G * nq;
 
   const int warp = warp_id();
@@ -163,16 +171,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars.kv_full, 1);
     for (int i = 0; i < kQStages; ++i) {
       mbar_init(&bars.q_full[i], 1);
-      mbar_init(&bars.q_empty[i], 2);   // one commit from each MMA issuer
+      mbar_init(&bars.q_empty[i], 3);   // S^T, dP^T and dV/dK issuers read the stage
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars.sdp_full[i], 1);
+      mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.dp_full[i], 1);
+      mbar_init(&bars.p_full[i], kComputeWarps * 32);
       mbar_init(&bars.ds_full[i], kComputeWarps * 32);
+      mbar_init(&bars.kv_done[i], 1);
       mbar_init(&bars.ds_empty[i], 1);
       mbar_init(&bars.dq_full[i], 1);
       mbar_init(&bars.dq_empty[i], 4 * 32);
-      mbar_init(&bars.mma_final[i], 1);
     }
+    for (int i = 0; i < 3; ++i) mbar_init(&bars.mma_final[i], 1);
     mbar_init(&bars.acc_done, 1);
     fence_barrier_init();
   }
@@ -189,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_u32(smem + kOffQ);
   const uint32_t sDO = smem_u32(smem + kOffDO);
   const uint32_t sDS = smem_u32(smem + kOffDS);
-  float* stat = reinterpret_cast<float*>(smem + kOffStat);  // [stage][L 64 | Delta 64]
+  float* stat = reinterpret_cast<float*>(smem + kOffStat);  // [stage][-L log2 e 64 | Delta 64]
 
   auto step_head = [&](int n) { return g * p.G + n / nq; };
   auto step_qtile = [&](int n) { return qi_first + n % nq; };
@@ -215,14 +226,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qi = step_qtile(n);
         if (!wd.wait(&bars.q_empty[st], ph ^ 1)) break;
         const int qrow = b * p.q_len + qi * kBQ;
-        const int64_t srow = (static_cast<int64_t>(b) * p.Hq + h) * p.q_len + qi * kBQ;
+        const int64_t sblk = ((static_cast<int64_t>(b) * p.Hq + h) * p.n_q64 + qi) * (2 * kBQ);
         mbar_arrive_expect_tx(&bars.q_full[st], 2 * kQTileBytes + kStatBytes);
         tma_load_3d(smem + kOffQ + st * kQTileBytes, &map_q, &bars.q_full[st], 0, h, qrow);
         tma_load_3d(smem + kOffQ + st * kQTileBytes + kQHalf, &map_q, &bars.q_full[st], 64, h, qrow);
         tma_load_3d(smem + kOffDO + st * kQTileBytes, &map_do, &bars.q_full[st], 0, h, qrow);
         tma_load_3d(smem + kOffDO + st * kQTileBytes + kQHalf, &map_do, &bars.q_full[st], 64, h, qrow);
-        bulk_load(stat + st * 2 * kBQ, p.lse + srow, kBQ * 4, &bars.q_full[st]);
-        bulk_load(stat + st * 2 * kBQ + kBQ, p.delta + srow, kBQ * 4, &bars.q_full[st]);
+        bulk_load(stat + st * 2 * kBQ, p.stats + sblk, kStatBytes, &bars.q_full[st]);
         issued[st] = n + 1;
       }
       if (wd.aborted()) {
@@ -231,69 +241,67 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (issued[st] > 0) wd.drain(&bars.q_full[st], ((issued[st] - 1) / kQStages) & 1, 1000000);
       }
     }
-  } else if (warp == 1 || warp == kIssuerB) {
+  } else if (warp == 1 || warp == kIssuerKV || warp == kIssuerDP) {
     // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
       const uint32_t idesc_sdp = make_idesc_bf16(kBK, kBQ, false, false);  // M128 N64, K-major both
       const uint32_t idesc_kv = make_idesc_bf16(kBK, kD, false, true);     // M128 N128, B MN-major
       const uint32_t idesc_dq = make_idesc_bf16(kD, kBQ, true, true);      // M128 N64, both MN-major
-      const bool is_a = (warp == 1);
-      bool ok = true;
-      if (is_a) {
-        // ---- issuer A: S^T(n) and dP^T(n) into buffer n&1, as early as the
-        // Q/dO stage has landed and step n-2 has released the buffer
-        const uint64_t k_kmaj = make_desc_sw128(sK, 16, 1024);
-        const uint64_t v_kmaj = make_desc_sw128(sV, 16, 1024);
-        const uint64_t q_kmaj0 = make_desc_sw128(sQ, 16, 1024);
-        const uint64_t do_kmaj0 = make_desc_sw128(sDO, 16, 1024);
-        ok = wd.wait(&bars.kv_full, 0);
+      // role 0: S^T (warp 1), role 1: dV, dK, dQ^T (kIssuerKV), role 2: dP^T
+      const int role = warp == 1 ? 0 : (warp == kIssuerKV ? 1 : 2);
+      bool ok = wd.wait(&bars.kv_full, 0);
+      if (role != 1) {
+        // ---- S^T(n) (role 0) or dP^T(n) (role 2) into buffer n&1 as soon as
+        // the Q/dO stage has landed and step n-2 has released that half
+        const bool is_s = role == 0;
+        const uint64_t a_kmaj = make_desc_sw128(is_s ? sK : sV, 16, 1024);
+        const uint64_t b_kmaj0 = make_desc_sw128(is_s ? sQ : sDO, 16, 1024);
+        uint64_t* full = is_s ? bars.s_full : bars.dp_full;
+        uint64_t* release = is_s ? bars.kv_done : bars.dq_empty;
+        const uint32_t off = is_s ? kOffS : kOffDP;
         for (int n = 0; ok && n < n_steps; ++n) {
           const int st = n % kQStages;
           const int bb = n & 1;
           if (!(ok = wd.wait(&bars.q_full[st], (n / kQStages) & 1))) break;
-          if (n >= 2 && !(ok = wd.wait(&bars.dq_empty[bb], ((n - 2) >> 1) & 1))) break;
+          if (n >= 2 && !(ok = wd.wait(&release[bb], ((n - 2) >> 1) & 1))) break;
           tc_fence_after_sync();
-          const uint64_t qd = q_kmaj0 + static_cast<uint64_t>(st * (kQTileBytes >> 4));
-          const uint64_t dd = do_kmaj0 + static_cast<uint64_t>(st * (kQTileBytes >> 4));
-          const uint32_t cb = tmem + col_buf(bb);
+          const uint64_t bd = b_kmaj0 + static_cast<uint64_t>(st * (kQTileBytes >> 4));
+          const uint32_t d = tmem + col_buf(bb) + off;
 #pragma unroll
-          for (int ks = 0; ks < kD / 16; ++ks) {
-            umma_bf16_ss(cb + kOffS, k_kmaj + kmajor_off(kKVHalf, ks), qd + kmajor_off(kQHalf, ks), idesc_sdp,
+          for (int ks = 0; ks < kD / 16; ++ks)
+            umma_bf16_ss(d, a_kmaj + kmajor_off(kKVHalf, ks), bd + kmajor_off(kQHalf, ks), idesc_sdp,
                          ks > 0 ? 1u : 0u);
-            umma_bf16_ss(cb + kOffDP, v_kmaj + kmajor_off(kKVHalf, ks), dd + kmajor_off(kQHalf, ks), idesc_sdp,
-                         ks > 0 ? 1u : 0u);
-          }
-          umma_commit(&bars.sdp_full[bb]);
-          umma_commit(&bars.q_empty[st]);   // issuer A's readers of the stage are done
+          umma_commit(&full[bb]);
+          umma_commit(&bars.q_empty[st]);
         }
-        umma_commit(&bars.mma_final[0]);
-        wd.drain(&bars.mma_final[0], 0, 4000000);
       } else {
-        // ---- issuer B: dV, dK, then dQ^T of step n once P^T/dS^T are written
-        const uint64_t k_mn = make_desc_sw128(sK, kKVHalf, 1024);
+        // ---- dV += P^T dO once P^T(n) is written; dK += dS^T Q and
+        // dQ^T(n) = K^T dS^T (over the already read dP^T half) once dS^T(n) is
         const uint64_t q_mn0 = make_desc_sw128(sQ, kQHalf, 1024);
         const uint64_t do_mn0 = make_desc_sw128(sDO, kQHalf, 1024);
+        const uint64_t k_mn = make_desc_sw128(sK, kKVHalf, 1024);
         const uint64_t ds_mn0 = make_desc_sw128(sDS, kPTileBytes, 1024);
         for (int n = 0; ok && n < n_steps; ++n) {
           const int st = n % kQStages;
           const int bb = n & 1;
+          const uint32_t cb = tmem + col_buf(bb);
+          if (!(ok = wd.wait(&bars.p_full[bb], (n >> 1) & 1))) break;
+          tc_fence_after_sync();
+          const uint64_t dm = do_mn0 + static_cast<uint64_t>(st * (kQTileBytes >> 4));
+#pragma unroll
+          for (int ks = 0; ks < kBQ / 16; ++ks)
+            umma_bf16_ts(tmem + kColDV, cb + kOffS + pair_col(ks), dm + mnmajor_off(ks), idesc_kv,
+                         (n > 0 || ks > 0) ? 1u : 0u);
           if (!(ok = wd.wait(&bars.ds_full[bb], (n >> 1) & 1))) break;
           tc_fence_after_sync();
           const uint64_t qm = q_mn0 + static_cast<uint64_t>(st * (kQTileBytes >> 4));
-          const uint64_t dm = do_mn0 + static_cast<uint64_t>(st * (kQTileBytes >> 4));
-          const uint64_t sm = ds_mn0 + static_cast<uint64_t>(bb * (kPTileBytes >> 4));
-          const uint32_t cb = tmem + col_buf(bb);
-          // dV += P^T dO ; dK += dS^T Q  (K = 64 query rows: 4 steps), interleaved
 #pragma unroll
-          for (int ks = 0; ks < kBQ / 16; ++ks) {
-            umma_bf16_ts(tmem + kColDV, cb + kOffS + pair_col(ks), dm + mnmajor_off(ks), idesc_kv,
+          for (int ks = 0; ks < kBQ / 16; ++ks)
+            umma_bf16_ts(tmem + kColDK, cb + kOffS + pair_col(ks) + kDSPairs, qm + mnmajor_off(ks), idesc_kv,
                          (n > 0 || ks > 0) ? 1u : 0u);
-            umma_bf16_ts(tmem + kColDK, cb + kOffDP + pair_col(ks), qm + mnmajor_off(ks), idesc_kv,
-                         (n > 0 || ks > 0) ? 1u : 0u);
-          }
-          umma_commit(&bars.q_empty[st]);   // issuer B's readers of the stage are done
-          // dQ^T = K^T dS^T (K = 128 keys) over the dP^T half: issued after dK,
-          // which read dS^T there (one thread's MMAs run in issue order)
+          umma_commit(&bars.kv_done[bb]);
+          umma_commit(&bars.q_empty[st]);
+          const uint64_t sm = ds_mn0 + static_cast<uint64_t>(bb * (kPTileBytes >> 4));
 #pragma unroll
           for (int ks = 0; ks < kBK / 16; ++ks)
             umma_bf16_ss(cb + kOffDP, k_mn + mnmajor_off(ks), sm + mnmajor_off(ks), idesc_dq, ks > 0 ? 1u : 0u);
@@ -301,9 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(&bars.ds_empty[bb]);
         }
         umma_commit(&bars.acc_done);
-        umma_commit(&bars.mma_final[1]);
-        wd.drain(&bars.mma_final[1], 0, 4000000);
       }
+      umma_commit(&bars.mma_final[role]);
+      wd.drain(&bars.mma_final[role], 0, 4000000);
     }
   } else if (warp < 2 + kComputeWarps) {
     // ------------------------------------------------------------ P / dS
@@ -315,48 +323,74 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const int key = kb + kr;
     const int c_off = half * 32;                        // first query column of this warp
+    const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
     bool ok = true;
     for (int n = 0; n < n_steps; ++n) {
       const int st = n % kQStages;
       const int bb = n & 1;
       const int qi = step_qtile(n);
-      // the L/Delta statistics of the stage first: they load while S^T/dP^T compute
+      // -L log2(e) of the stage first: it loads while S^T computes
       if (!(ok = warp_wait(wd, &bars.q_full[st], (n / kQStages) & 1))) break;
       const float4* L4 = reinterpret_cast<const float4*>(stat + st * 2 * kBQ + c_off);
       const float4* D4 = reinterpret_cast<const float4*>(stat + st * 2 * kBQ + kBQ + c_off);
-      float lse2[32], dl[32];
+      uint64_t nl2[16];                                 // pairs of query rows
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float4 l = L4[j], dd = D4[j];
-        lse2[4 * j] = -l.x * kLog2e; lse2[4 * j + 1] = -l.y * kLog2e;
-        lse2[4 * j + 2] = -l.z * kLog2e; lse2[4 * j + 3] = -l.w * kLog2e;
-        dl[4 * j] = dd.x; dl[4 * j + 1] = dd.y; dl[4 * j + 2] = dd.z; dl[4 * j + 3] = dd.w;
+        const float4 l = L4[j];
+        nl2[2 * j] = f2_pack(l.x, l.y);
+        nl2[2 * j + 1] = f2_pack(l.z, l.w);
       }
-      if (!(ok = warp_wait(wd, &bars.sdp_full[bb], (n >> 1) & 1))) break;
+      if (!(ok = warp_wait(wd, &bars.s_full[bb], (n >> 1) & 1))) break;
       tc_fence_after_sync();
       const uint32_t cb = tmem + lane_base + col_buf(bb);
-      uint32_t rs[32], rp[32];
-      tmem_ld32(cb + kOffS + c_off, rs);
-      tmem_ld32(cb + kOffDP + c_off, rp);
-      const bool masked = diag_tile && (qi - qi_first) < 2;
+      uint32_t r[32];
+      tmem_ld32(cb + kOffS + c_off, r);
       const int q_abs0 = p.q_start + qi * kBQ + c_off;  // absolute row of this warp's column 0
+      const bool masked = kb + kBK - 1 > q_abs0;        // some key of the tile follows some row
       tmem_ld_wait();
-      uint32_t pp[16], pk[16];                          // packed bf16 pairs of P^T and dS^T
+      // P = 2^(s scale log2(e) - L log2(e)), exactly 0 on padding rows (-inf);
+      // kept in fp32 for dS
+      uint64_t p2[16];
+      uint32_t pk[16];                                  // packed bf16 pairs
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        float p0 = ex2(fmaf(__uint_as_float(rs[j]), p.scale_log2, lse2[j]));
-        float p1 = ex2(fmaf(__uint_as_float(rs[j + 1]), p.scale_log2, lse2[j + 1]));
+      for (int j = 0; j < 16; ++j) {
+        const uint64_t x = f2_fma(f2_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), scale2, nl2[j]);
+        float x0, x1;
+        f2_unpack(x, x0, x1);
+        float p0 = ex2(x0), p1 = ex2(x1);
         if (masked) {
-          if (key > q_abs0 + j) p0 = 0.f;
-          if (key > q_abs0 + j + 1) p1 = 0.f;
+          if (key > q_abs0 + 2 * j) p0 = 0.f;
+          if (key > q_abs0 + 2 * j + 1) p1 = 0.f;
         }
-        pp[j / 2] = pack_bf16x2(p0, p1);
-        pk[j / 2] = pack_bf16x2(p0 * (__uint_as_float(rp[j]) - dl[j]),
-                                p1 * (__uint_as_float(rp[j + 1]) - dl[j + 1]));
+        p2[j] = f2_pack(p0, p1);
+        pk[j] = pack_bf16x2(p0, p1);
       }
-      // P^T/dS^T pairs back over this warp's own S^T/dP^T columns
-      tmem_st16(cb + kOffS + c_off, pp);
-      tmem_st16(cb + kOffDP + c_off, pk);
+      // P^T pairs over the first 16 of this warp's S^T columns: dV can start
+      tmem_st16(cb + kOffS + c_off, pk);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars.p_full[bb]);
+      // dS = P o (dP - Delta)
+      if (!(ok = warp_wait(wd, &bars.dp_full[bb], (n >> 1) & 1))) break;
+      tc_fence_after_sync();
+      tmem_ld32(cb + kOffDP + c_off, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 dd = D4[j];
+        const uint64_t a0 = f2_mul(p2[2 * j], f2_sub(f2_pack(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1])),
+                                                     f2_pack(dd.x, dd.y)));
+        const uint64_t a1 = f2_mul(p2[2 * j + 1],
+                                   f2_sub(f2_pack(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])),
+                                          f2_pack(dd.z, dd.w)));
+        float u0, u1, u2, u3;
+        f2_unpack(a0, u0, u1);
+        f2_unpack(a1, u2, u3);
+        pk[2 * j] = pack_bf16x2(u0, u1);
+        pk[2 * j + 1] = pack_bf16x2(u2, u3);
+      }
+      // dS^T pairs over the last 16 of this warp's S^T columns
+      tmem_st16(cb + kOffS + c_off + kDSPairs, pk);
       // dS^T row segment to shared memory (B operand of dQ^T) once dQ^T of
       // step n-2 has read that buffer: 128-byte rows, 128-byte swizzle inside
       // 8-row groups; this warp writes 16-byte chunks 4*half .. 4*half+3
@@ -374,8 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- epilogue: this tile's dK (half 0) or dV (half 1) rows into the running sums
     if (ok) ok = warp_wait(wd, &bars.acc_done, 0);
-    if (ok) {
+    if (ok) {                                           // warp-uniform: the TMEM loads are .sync.aligned
       tc_fence_after_sync();
+      const bool store = key < q_end;                   // keys of a partial last tile past the chunk are dropped
       const int64_t row = (static_cast<int64_t>(b) * p.T + key) * p.Hkv + g;
       float4* dst = reinterpret_cast<float4*>((half == 0 ? p.dk : p.dv) + row * kD);
       const uint32_t col = half == 0 ? kColDK : kColDV;
@@ -387,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_base + col + c0 + 32, r1);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
+        for (int j = 0; j < 32 && store; j += 4) {
           float4 a = dst[(c0 + j) / 4];
           a.x += f * __uint_as_float(r0[j]);
           a.y += f * __uint_as_float(r0[j + 1]);
@@ -396,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           dst[(c0 + j) / 4] = a;
         }
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
+        for (int j = 0; j < 32 && store; j += 4) {
           float4 a = dst[(c0 + 32 + j) / 4];
           a.x += f * __uint_as_float(r1[j]);
           a.y += f * __uint_as_float(r1[j + 1]);
@@ -425,10 +460,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qi = step_qtile(n);
       float* base = p.dq + ((static_cast<int64_t>(b) * p.q_len + qi * kBQ) * p.Hq + h) * kD + dcol;
       const int64_t rstride = static_cast<int64_t>(p.Hq) * kD;
+      const int rows = p.q_len - qi * kBQ;              // rows of this query tile inside the chunk
+      if (rows >= kBQ) {
+        // full tile: 64 back-to-back reductions (a per-row predicate here
+        // halved the kernel's speed)
 #pragma unroll
-      for (int c = 0; c < 32; ++c) atomicAdd(base + c * rstride, p.scale * __uint_as_float(r0[c]));
+        for (int c = 0; c < 32; ++c) atomicAdd(base + c * rstride, p.scale * __uint_as_float(r0[c]));
 #pragma unroll
-      for (int c = 0; c < 32; ++c) atomicAdd(base + (c + 32) * rstride, p.scale * __uint_as_float(r1[c]));
+        for (int c = 0; c < 32; ++c) atomicAdd(base + (c + 32) * rstride, p.scale * __uint_as_float(r1[c]));
+      } else {
+        // partial last tile of a ragged chunk: rows past q_len are dropped
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (c < rows) atomicAdd(base + c * rstride, p.scale * __uint_as_float(r0[c]));
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (c + 32 < rows) atomicAdd(base + (c + 32) * rstride, p.scale * __uint_as_float(r1[c]));
+      }
     }
   }
 
@@ -442,9 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_bwd_bf16(const ChunkGeom& g, const Bf16BwdMaps& maps, const float* lse,
-                            const float* delta, float* dq, float* dk, float* dv, unsigned int* err,
-                            cudaStream_t s) {
+cudaError_t launch_bwd_bf16(const ChunkGeom& g, const Bf16BwdMaps& maps, const float* stats,
+                            float* dq, float* dk, float* dv, unsigned int* err, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(bwd_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemAlloc);
   if (e != cudaSuccess) return e;
@@ -457,11 +504,11 @@ cudaError_t launch_bwd_bf16(const ChunkGeom& g, const Bf16BwdMaps& maps, const f
   p.T = static_cast<int>(g.T);
   p.q_start = static_cast<int>(g.q_start);
   p.kv_begin = static_cast<int>(g.kv_begin);
-  p.n_ktiles = static_cast<int>((g.q_start + g.q_len - g.kv_begin) / kBK);
+  p.n_ktiles = static_cast<int>((g.q_start + g.q_len - g.kv_begin + kBK - 1) / kBK);
+  p.n_q64 = static_cast<int>((g.q_len + kBQ - 1) / kBQ);
   p.scale = g.scale;
-  p.scale_log2 = g.scale * kLog2e;
-  p.lse = lse;
-  p.delta = delta;
+  p.scale_log2 = g.scale * 1.4426950408889634f;
+  p.stats = stats;
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;

@@ -24,7 +24,8 @@
 // warps, and each SM sub-partition runs two softmax warps.  P is written back
 // into TMEM (over the S values just read) and never touches shared memory.
 // TMEM: S double-buffered (2 x 128 columns), O_0 and O_1 (128 columns each).
-// Only the last (diagonal) key tile carries the causal mask.  The running
+// Only key tiles that reach past the tile's first query row carry the causal
+// mask (one or two tiles, since chunks may start anywhere).  The running
 // maxima are rescaled lazily: O_h and l_h are only corrected when a row max
 // grows by more than 2^8 (P stays below 256).
 #include <cuda_bf16.h>
@@ -127,7 +128,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = idx / p.Hq;
   const int g = h / p.G;
   const int q0 = p.q_start + qt * kBM;                 // absolute row of query 0
-  const int n_kv = (q0 + kBM - p.kv_begin) / kBN;      // key tiles, last one diagonal
+  // keys [kv_begin, min(q0 + 128, q_end)) in 128-key tiles; rows of a partial
+  // last query tile past q_end are computed on whatever the copies bring and
+  // never stored
+  const int q_end = p.q_start + p.q_len;
+  const int n_kv = (min(q0 + kBM, q_end) - p.kv_begin + kBN - 1) / kBN;
 
   const int warp = warp_id();
   const int lane = lane_id();
@@ -269,13 +274,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem + lane_base + kColS + st * kBN + half * 64, ra);
       tmem_ld32(tmem + lane_base + kColS + st * kBN + half * 64 + 32, rb);
       tmem_ld_wait();
-      const bool diag = (t == n_kv - 1);
-      if (diag) {
-        // diagonal tile: key c (absolute q0 + c) is visible to row r iff c <= r
+      const int key0 = p.kv_begin + t * kBN;              // absolute first key of the tile
+      if (key0 + kBN - 1 > q0) {
+        // the tile reaches past query row 0: key key0 + c is visible to row r
+        // iff key0 + c <= q0 + r, i.e. c <= lim for this thread's keys
+        const int lim = q0 + row - key0 - half * 64;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          if (half * 64 + j > row) ra[j] = __float_as_uint(-INFINITY);
-          if (half * 64 + 32 + j > row) rb[j] = __float_as_uint(-INFINITY);
+          if (j > lim) ra[j] = __float_as_uint(-INFINITY);
+          if (32 + j > lim) rb[j] = __float_as_uint(-INFINITY);
         }
       }
       float mx = fmax3(__uint_as_float(ra[0]), __uint_as_float(ra[1]), __uint_as_float(rb[0]));
@@ -354,7 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     merge_m[half][row] = m_run;
     merge_l[half][row] = l_run;
     named_barrier_sync(1, kSoftmaxWarps * 32);
-    if (ok && !wd.aborted()) {
+    const int qrow = qt * kBM + row;                    // chunk-local row
+    const bool store = qrow < p.q_len;                  // rows of a partial last tile past q_len are dropped
+    if (ok && !wd.aborted()) {                          // warp-uniform: the TMEM loads are .sync.aligned
       tc_fence_after_sync();
       const float m0 = merge_m[0][row], m1 = merge_m[1][row];
       const float M = fmaxf(m0, m1);
@@ -363,7 +372,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float L = merge_l[0][row] * a0 + merge_l[1][row] * a1;
       const float inv = 1.f / L;
       const float f0 = a0 * inv, f1 = a1 * inv;
-      const int qrow = qt * kBM + row;
       // this warp writes head-dim columns [64 half, 64 half + 64) of the row
       uint4* orow = reinterpret_cast<uint4*>(p.o + ((static_cast<int64_t>(b) * p.q_len + qrow) * p.Hq + h) * kD +
                                              half * 64);
@@ -384,10 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           q.y = pack_bf16x2(v[2], v[3]);
           q.z = pack_bf16x2(v[4], v[5]);
           q.w = pack_bf16x2(v[6], v[7]);
-          orow[(c0 + j) / 8] = q;
+          if (store) orow[(c0 + j) / 8] = q;
         }
       }
-      if (half == 0)
+      if (half == 0 && store)
         p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.q_len + qrow] = (M + __log2f(L)) * kLn2;
     }
   }
@@ -416,7 +424,7 @@ cudaError_t launch_fwd_bf16(const ChunkGeom& g, const Bf16FwdMaps& maps, void* o
   p.T = static_cast<int>(g.T);
   p.q_start = static_cast<int>(g.q_start);
   p.kv_begin = static_cast<int>(g.kv_begin);
-  p.n_qtiles = static_cast<int>(g.q_len / kBM);
+  p.n_qtiles = static_cast<int>((g.q_len + kBM - 1) / kBM);
   p.scale_log2 = g.scale * kLog2e;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;

@@ -25,9 +25,12 @@ cudaError_t launch_bwd_f32(const ChunkGeom& g, const float* q, const float* k, c
                            const float* lse, const float* d_o, const float* delta, float* dq,
                            float* dk, float* dv, unsigned int* err, cudaStream_t s);
 
-// ---- Delta = rowsum(dO o O) (+ zero dq when `zero_dq`), any input type ----
-cudaError_t launch_bwd_prep_bf16(const ChunkGeom& g, const void* o, const void* d_o,
-                                 float* delta, float* dq_to_zero, cudaStream_t s);
+// ---- Delta = rowsum(dO o O) and the backward row statistics ---------------
+// bf16 path: per 64-row query tile, -L log2(e) and Delta side by side in a
+// padded [B, Hq, ceil(q_len / 64), 2, 64] float32 array (padding rows -inf, 0);
+// also zeroes dq.
+cudaError_t launch_bwd_stats_bf16(const ChunkGeom& g, const void* o, const void* d_o,
+                                  const float* lse, float* stats, float* dq, cudaStream_t s);
 cudaError_t launch_bwd_prep_f32(const ChunkGeom& g, const float* o, const float* d_o,
                                 float* delta, cudaStream_t s);
 
@@ -44,8 +47,8 @@ struct Bf16BwdMaps {
 };
 cudaError_t launch_fwd_bf16(const ChunkGeom& g, const Bf16FwdMaps& maps, void* o, float* lse,
                             unsigned int* err, cudaStream_t s);
-cudaError_t launch_bwd_bf16(const ChunkGeom& g, const Bf16BwdMaps& maps, const float* lse,
-                            const float* delta, float* dq, float* dk, float* dv,
-                            unsigned int* err, cudaStream_t s);
+// `stats` as written by launch_bwd_stats_bf16.
+cudaError_t launch_bwd_bf16(const ChunkGeom& g, const Bf16BwdMaps& maps, const float* stats,
+                            float* dq, float* dk, float* dv, unsigned int* err, cudaStream_t s);
 
 }  // namespace seqattn

@@ -131,9 +131,6 @@ seqattn_status check_chunk(const seqattn_problem* pb, int64_t q_start, int64_t q
   if (pb->dtype == SEQATTN_BF16) {
     if (pb->head_dim != 128)
       return fail(SEQATTN_ERR_UNSUPPORTED, "bf16 path needs head_dim 128 (got %d)", pb->head_dim);
-    if (q_start % 128 || q_len % 128 || prefix_len % 128)
-      return fail(SEQATTN_ERR_UNSUPPORTED,
-                  "bf16 path needs q_start, q_len and prefix_len to be multiples of 128");
   }
   g->B = pb->batch;
   g->Hq = pb->num_q_heads;
@@ -158,9 +155,12 @@ seqattn_status check_ptrs(std::initializer_list<std::pair<const void*, const cha
 }
 
 size_t workspace_bytes(const seqattn_problem* pb, int64_t q_len) {
-  // Delta [B, Hq, q_len] float32, rounded up to 256 bytes.
-  const size_t delta = static_cast<size_t>(pb->batch) * pb->num_q_heads * q_len * sizeof(float);
-  return (delta + 255) & ~static_cast<size_t>(255);
+  // float32: Delta [B, Hq, q_len].  bf16: -L log2(e) and Delta per 64-row
+  // query tile, [B, Hq, ceil(q_len / 64), 2, 64].  Rounded up to 256 bytes.
+  const size_t rows = pb->dtype == SEQATTN_BF16 ? static_cast<size_t>((q_len + 63) / 64) * 128
+                                                : static_cast<size_t>(q_len);
+  const size_t bytes = static_cast<size_t>(pb->batch) * pb->num_q_heads * rows * sizeof(float);
+  return (bytes + 255) & ~static_cast<size_t>(255);
 }
 
 }  // namespace
@@ -233,9 +233,9 @@ seqattn_status seqattn_chunk_bwd(const seqattn_problem* pb, int64_t q_start, int
       !make_map(&maps.k, k, g.d, g.Hkv, static_cast<int64_t>(g.B) * g.T, 128) ||
       !make_map(&maps.v, v, g.d, g.Hkv, static_cast<int64_t>(g.B) * g.T, 128))
     return fail(SEQATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the backward operands");
-  e = launch_bwd_prep_bf16(g, o, d_o, delta, dq, st);
-  if (e != cudaSuccess) return cuda_fail(e, "bwd_prep launch");
-  e = launch_bwd_bf16(g, maps, lse, delta, dq, dk_accum, dv_accum, err, st);
+  e = launch_bwd_stats_bf16(g, o, d_o, lse, delta, dq, st);
+  if (e != cudaSuccess) return cuda_fail(e, "bwd_stats launch");
+  e = launch_bwd_bf16(g, maps, delta, dq, dk_accum, dv_accum, err, st);
   return e == cudaSuccess ? ok() : cuda_fail(e, "bwd_bf16 launch");
 }
 
@@ -301,8 +301,8 @@ const char* seqattn_last_error(void) { return t_last_error.c_str(); }
 namespace seqattn {
 namespace {
 
-// Delta scratch: B * Hq * q_len floats at most (4 MiB on every GPU that
-// loads the library, held until the process exits).
+// Row-statistics scratch (what seqattn_bwd_workspace_size asks for, at most
+// 4 MiB) on every GPU that loads the library, held until the process exits.
 static __device__ __align__(256) float g_noalloc_delta[SEQATTN_NOALLOC_MAX_DELTA];
 
 float* g_noalloc_ptr[kMaxDevices] = {};
@@ -341,12 +341,12 @@ extern "C" seqattn_status seqattn_chunk_bwd_noalloc(
   s = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}, {d_o, "d_o"}, {dq, "dq"},
                   {dk_accum, "dk_accum"}, {dv_accum, "dv_accum"}});
   if (s != SEQATTN_OK) return s;
-  const int64_t rows = static_cast<int64_t>(pb->batch) * pb->num_q_heads * q_len;
-  if (rows > SEQATTN_NOALLOC_MAX_DELTA)
+  const size_t need = workspace_bytes(pb, q_len);
+  if (need > sizeof(float) * static_cast<size_t>(SEQATTN_NOALLOC_MAX_DELTA))
     return fail(SEQATTN_ERR_INVALID_ARG,
-                "batch * num_q_heads * q_len = %lld exceeds the fixed scratch of %d rows of "
-                "seqattn_chunk_bwd_noalloc; use seqattn_chunk_bwd with a workspace",
-                (long long)rows, SEQATTN_NOALLOC_MAX_DELTA);
+                "this chunk needs %zu bytes of row statistics, more than the fixed scratch of %d "
+                "floats of seqattn_chunk_bwd_noalloc; use seqattn_chunk_bwd with a workspace",
+                need, SEQATTN_NOALLOC_MAX_DELTA);
   float* delta = nullptr;
   cudaError_t e = noalloc_scratch(&delta);
   if (e != cudaSuccess) return cuda_fail(e, "scratch address");
@@ -368,8 +368,8 @@ extern "C" seqattn_status seqattn_chunk_bwd_noalloc(
       !make_map(&maps.k, k, g.d, g.Hkv, static_cast<int64_t>(g.B) * g.T, 128) ||
       !make_map(&maps.v, v, g.d, g.Hkv, static_cast<int64_t>(g.B) * g.T, 128))
     return fail(SEQATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the backward operands");
-  e = launch_bwd_prep_bf16(g, o, d_o, delta, dq, st);
-  if (e != cudaSuccess) return cuda_fail(e, "bwd_prep launch");
-  e = launch_bwd_bf16(g, maps, lse, delta, dq, dk_accum, dv_accum, err, st);
+  e = launch_bwd_stats_bf16(g, o, d_o, lse, delta, dq, st);
+  if (e != cudaSuccess) return cuda_fail(e, "bwd_stats launch");
+  e = launch_bwd_bf16(g, maps, delta, dq, dk_accum, dv_accum, err, st);
   return e == cudaSuccess ? ok() : cuda_fail(e, "bwd_bf16 launch");
 }

@@ -1,7 +1,7 @@
 // simt_f32.cu -- the float32 path of the chunk calls (plain FMA arithmetic,
 // no tensor cores, so results stay within float32 rounding of the exact
-// value), the Delta preprocess shared by both paths, and the accumulator
-// zero fill.
+// value), the Delta preprocess of that path, the row-statistics pre-pass of
+// the bf16 tensor-core backward, and the accumulator zero fill.
 //
 // Operation: the partitioned causal attention of the StreamBP review page
 // (Property 3.1 and Eqs. (12)-(14) named in its "Circularity Check"):
@@ -259,10 +259,6 @@ template <typename T>
 __device__ __forceinline__ float ld_f(const T* p);
 template <>
 __device__ __forceinline__ float ld_f<float>(const float* p) { return *p; }
-template <>
-__device__ __forceinline__ float ld_f<__nv_bfloat16>(const __nv_bfloat16* p) {
-  return __bfloat162float(*p);
-}
 
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(ChunkGeom g, const T* __restrict__ o,
@@ -288,6 +284,50 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(ChunkGeom g, const T* __r
     float* z = dq_to_zero + warp * g.d;
     for (int e = lane; e < g.d; e += 32) z[e] = 0.f;
   }
+}
+
+// bf16 tensor-core backward statistics, one warp per (padded row, head):
+// stats[((b Hq + h) n64 + r / 64) * 128 + r % 64]      = -L[b, h, r] log2(e)
+// stats[((b Hq + h) n64 + r / 64) * 128 + 64 + r % 64] = Delta[b, h, r]
+// for r < q_len, and -inf / 0 for the padding rows q_len <= r < 64 n64, so a
+// padding row's P = 2^(s scale log2(e) - inf) is exactly 0.  Each 64-row query
+// tile's statistics are one contiguous 512-byte block.  Zeroes dq rows too.
+__global__ void __launch_bounds__(256) bwd_stats_bf16_kernel(ChunkGeom g, int n64,
+                                                             const __nv_bfloat16* __restrict__ o,
+                                                             const __nv_bfloat16* __restrict__ d_o,
+                                                             const float* __restrict__ lse,
+                                                             float* __restrict__ stats,
+                                                             float* __restrict__ dq) {
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t q_pad = static_cast<int64_t>(n64) * 64;
+  const int64_t n_rows = static_cast<int64_t>(g.B) * q_pad * g.Hq;  // (b, r, h) rows
+  if (warp >= n_rows) return;
+  const int h = static_cast<int>(warp % g.Hq);
+  const int64_t br = warp / g.Hq;
+  const int b = static_cast<int>(br / q_pad);
+  const int64_t r = br % q_pad;
+  float* dst = stats + ((static_cast<int64_t>(b) * g.Hq + h) * n64 + r / 64) * 128 + (r % 64);
+  if (r >= g.q_len) {
+    if (lane == 0) {
+      dst[0] = -INFINITY;
+      dst[64] = 0.f;
+    }
+    return;
+  }
+  const int64_t row = (static_cast<int64_t>(b) * g.q_len + r) * g.Hq + h;
+  const __nv_bfloat16* orow = o + row * g.d;
+  const __nv_bfloat16* drow = d_o + row * g.d;
+  float s = 0.f;
+  for (int e = lane; e < g.d; e += 32) s = fmaf(__bfloat162float(orow[e]), __bfloat162float(drow[e]), s);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane == 0) {
+    dst[0] = -lse[(static_cast<int64_t>(b) * g.Hq + h) * g.q_len + r] * 1.4426950408889634f;
+    dst[64] = s;
+  }
+  float* z = dq + row * g.d;
+  for (int e = lane; e < g.d; e += 32) z[e] = 0.f;
 }
 
 __global__ void zero2_kernel(float4* __restrict__ a, float4* __restrict__ b, int64_t n4) {
@@ -372,10 +412,16 @@ cudaError_t launch_bwd_f32(const ChunkGeom& g, const float* q, const float* k, c
                    : bwd_f32_d<128>(g, q, k, v, lse, d_o, delta, dq, dk, dv, err, s);
 }
 
-cudaError_t launch_bwd_prep_bf16(const ChunkGeom& g, const void* o, const void* d_o, float* delta,
-                                 float* dq_to_zero, cudaStream_t s) {
-  return prep<__nv_bfloat16>(g, static_cast<const __nv_bfloat16*>(o),
-                             static_cast<const __nv_bfloat16*>(d_o), delta, dq_to_zero, s);
+cudaError_t launch_bwd_stats_bf16(const ChunkGeom& g, const void* o, const void* d_o,
+                                  const float* lse, float* stats, float* dq, cudaStream_t s) {
+  const int n64 = static_cast<int>((g.q_len + 63) / 64);
+  const int64_t rows = static_cast<int64_t>(g.B) * n64 * 64 * g.Hq;
+  const int threads = 256;
+  const int64_t blocks = (rows * 32 + threads - 1) / threads;
+  bwd_stats_bf16_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
+      g, n64, static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), lse, stats,
+      dq);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_prep_f32(const ChunkGeom& g, const float* o, const float* d_o, float* delta,

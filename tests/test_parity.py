@@ -182,6 +182,87 @@ def test_bf16_small_multi_tile():
         _bf16_group_check(w, cpu, bufs, chunk, range(Hkv))
 
 
+def _check_bf16_layer(B, T, Hq, Hkv, d, chunk, seed):
+    w = workloads.Workload("ragged", B, T, Hq, Hkv, d, "bf16", (chunk,), seed)
+    cpu = small_inputs(B, T, Hq, Hkv, d, "bf16", seed)
+    bufs = run_layer(*[x.cuda() for x in cpu], chunk)
+    _bf16_group_check(w, cpu, bufs, chunk, range(Hkv))
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,d,chunk", [
+    (2, 1000, 4, 2, 128, 500),   # the pages' partition size 500, batch 2
+    (1, 257, 8, 1, 128, 100),    # ragged 57-row tail, G=8
+    (1, 384, 2, 1, 128, 160),    # chunk starts off the 64/128 grid
+    (1, 200, 2, 2, 128, 200),    # one chunk (D=1) of 200 rows, MHA
+    (1, 70, 2, 1, 128, 1),       # one-row chunks
+])
+def test_bf16_ragged_shapes(B, T, Hq, Hkv, d, chunk):
+    _check_bf16_layer(B, T, Hq, Hkv, d, chunk, seed=12)
+
+
+def test_bf16_truncated_prefix_single_chunk():
+    """prefix_len < q_start: keys [q_start - prefix_len, q_start + r] only,
+    with every bound off the tile grid; accumulator rows outside the window
+    stay zero."""
+    B, T, Hq, Hkv, d = 2, 600, 4, 2, 128
+    cpu = small_inputs(B, T, Hq, Hkv, d, "bf16", 23)
+    q, k, v, do = (x.cuda() for x in cpu)
+    qs, c, p = 300, 130, 171
+    lse = torch.empty((B, Hq, c), device="cuda")
+    o_c = torch.empty((B, c, Hq, d), dtype=torch.bfloat16, device="cuda")
+    dq_c = torch.empty((B, c, Hq, d), device="cuda")
+    binding.chunk_fwd(q[:, qs:qs + c].contiguous(), k, v, o_c, lse, qs, p)
+    dk = torch.zeros(k.shape, device="cuda")
+    dv = torch.zeros(v.shape, device="cuda")
+    binding.chunk_bwd(q[:, qs:qs + c].contiguous(), k, v, o_c, lse, do[:, qs:qs + c].contiguous(),
+                      dq_c, dk, dv, qs, p)
+    binding.sync_status()
+    qn, kn, vn, don = (x.to(torch.float64).numpy() for x in cpu)
+    scale = d ** -0.5
+    ro, rl = oracle.chunk_forward(qn[:, qs:qs + c], kn, vn, qs, p, scale)
+    rdk, rdv = np.zeros(kn.shape), np.zeros(vn.shape)
+    rdq = oracle.chunk_backward(qn[:, qs:qs + c], kn, vn, ro, rl, don[:, qs:qs + c], qs, p, scale,
+                                rdk, rdv)
+    assert_bf16("O", cpu64(o_c), ro)
+    assert_bf16("LSE", cpu64(lse), rl)
+    assert_bf16("dQ", cpu64(dq_c), rdq)
+    assert_bf16("dK", cpu64(dk), rdk)
+    assert_bf16("dV", cpu64(dv), rdv)
+    assert float(dk[:, :qs - p].abs().max()) == 0.0 and float(dk[:, qs + c:].abs().max()) == 0.0
+    assert float(dv[:, :qs - p].abs().max()) == 0.0 and float(dv[:, qs + c:].abs().max()) == 0.0
+
+
+def test_bf16_ragged_guard_bands_untouched():
+    """A chunk of 200 rows (partial last 128-row and 64-row tiles) with its
+    outputs embedded in canary-filled buffers: forward and backward write
+    only inside their tensors."""
+    B, T, Hq, Hkv, d, qs, c = 1, 512, 4, 2, 128, 256, 200
+    cpu = small_inputs(B, T, Hq, Hkv, d, "bf16", 31)
+    q, k, v, do = (x.cuda() for x in cpu)
+    canary = 4096.0                                   # exact in bf16 and fp32
+    pad = 8192
+    n_o, n_l = B * c * Hq * d, B * Hq * c
+    big_o = torch.full((2 * pad + n_o,), canary, dtype=torch.bfloat16, device="cuda")
+    big_l = torch.full((2 * pad + n_l,), canary, device="cuda")
+    big_dq = torch.full((2 * pad + n_o,), canary, device="cuda")
+    n_kv = B * T * Hkv * d
+    big_dk = torch.full((2 * pad + n_kv,), canary, device="cuda")
+    o = big_o[pad:pad + n_o].view(B, c, Hq, d)
+    lse = big_l[pad:pad + n_l].view(B, Hq, c)
+    dq = big_dq[pad:pad + n_o].view(B, c, Hq, d)
+    dk = big_dk[pad:pad + n_kv].view(B, T, Hkv, d)
+    dk.zero_()
+    dv = torch.zeros(k.shape, device="cuda")
+    binding.chunk_fwd(q[:, qs:qs + c].contiguous(), k, v, o, lse, qs)
+    binding.chunk_bwd(q[:, qs:qs + c].contiguous(), k, v, o, lse, do[:, qs:qs + c].contiguous(),
+                      dq, dk, dv, qs)
+    binding.sync_status()
+    for name, big in (("o", big_o), ("lse", big_l), ("dq", big_dq), ("dk", big_dk)):
+        assert float((big[:pad].float() != canary).sum()) == 0, name
+        assert float((big[-pad:].float() != canary).sum()) == 0, name
+    assert float(dk[:, qs + c:].abs().max()) == 0.0 and float(dv[:, qs + c:].abs().max()) == 0.0
+
+
 def test_bf16_qwen3_4b_layer_two_groups():
     w = workloads.WORKLOADS["qwen3-4b-layer-t8192-c512"]
     cpu = inputs.layer_inputs(w)
