@@ -52,6 +52,7 @@ __all__ = [
     "chunk_forward",
     "chunk_backward",
     "chunked_layer",
+    "sparse_chunked_layer",
     "dense_causal_attention",
     "dense_causal_attention_grad",
     "row_forward",
@@ -170,6 +171,49 @@ def chunked_layer(q, k, v, do, chunk, scale, bwd_order="descending"):
         e = min(s + chunk, T)
         dq[:, s:e] = chunk_backward(q[:, s:e], k, v, o[:, s:e], lse[:, :, s:e],
                                     do[:, s:e], s, s, scale, dk, dv)
+    return o, lse, dq, dk, dv
+
+
+def sparse_chunked_layer(q, k, v, do, chunk, scale, selected, factor):
+    """SpaCO through the chunk calls (SeCO review page: "Referee Report",
+    Summary -- t of the k chunks are chosen for backpropagation and the relayed
+    KV-cache gradient is multiplied by k/t -- and its major comments on
+    Algorithm 2, whose compensation touches only the relayed cache gradient and
+    not a chunk's direct term, and on Section 6.4, which caps the factor at 2).
+
+    The forward (the inference pass that builds every cache) runs over all
+    chunks.  The backward visits chunks last to first.  A selected chunk i
+    first multiplies the gradient that later selected chunks relayed into its
+    own key/value rows by `factor`, then adds its own contributions over its
+    whole key range.  A chunk that is not selected is not backpropagated: its
+    rows, complete once every later chunk has run, are set to zero, since
+    nothing propagates from them.  `selected` (the sampled chunk indices) and
+    `factor` (min(k/t, 2) in the deployed method) are inputs.
+
+    Returns O, LSE, dQ (zero rows for chunks not selected), dK, dV (float64)."""
+    q, k, v, do = (_as64(x) for x in (q, k, v, do))
+    B, T, Hq, d = q.shape
+    starts = list(range(0, T, chunk))
+    chosen = set(int(i) for i in selected)
+    o = np.zeros_like(q)
+    lse = np.zeros((B, Hq, T))
+    for s in starts:
+        e = min(s + chunk, T)
+        o[:, s:e], lse[:, :, s:e] = chunk_forward(q[:, s:e], k, v, s, s, scale)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for i in reversed(range(len(starts))):
+        s = starts[i]
+        e = min(s + chunk, T)
+        if i in chosen:
+            dk[:, s:e] *= factor
+            dv[:, s:e] *= factor
+            dq[:, s:e] = chunk_backward(q[:, s:e], k, v, o[:, s:e], lse[:, :, s:e],
+                                        do[:, s:e], s, s, scale, dk, dv)
+        else:
+            dk[:, s:e] = 0.0
+            dv[:, s:e] = 0.0
     return o, lse, dq, dk, dv
 
 

@@ -284,6 +284,71 @@ def test_pins_catch_planted_mistakes():
     assert np.abs(o_t[:, :, :1] - o[:, :, :1]).max() > 1e-3
 
 
+# ---------------------------------------------------------------- SpaCO (sampled chunks)
+
+def _spaco_expected(q, k, v, do, chunk, scale, selected, factor):
+    """SpaCO's result composed by hand from the dense gradient: the gradient is
+    linear in dO, so chunk j's own contribution C_j is the dense gradient with
+    dO zeroed outside chunk j.  Rows of a selected chunk i receive
+    factor * sum_{selected j > i} C_j + C_i; rows of other chunks are zero;
+    dQ rows of a selected chunk come from its own dO only."""
+    B, T, Hq, d = q.shape
+    starts = list(range(0, T, chunk))
+    contrib = []
+    for s in starts:
+        e = min(s + chunk, T)
+        do_j = np.zeros_like(do)
+        do_j[:, s:e] = do[:, s:e]
+        contrib.append(oracle.dense_causal_attention_grad(q, k, v, do_j, scale))
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for i, s in enumerate(starts):
+        e = min(s + chunk, T)
+        if i not in selected:
+            continue
+        dq[:, s:e] = contrib[i][0][:, s:e]
+        later = [j for j in selected if j > i]
+        dk[:, s:e] = contrib[i][1][:, s:e] + factor * sum((contrib[j][1][:, s:e] for j in later), 0.0)
+        dv[:, s:e] = contrib[i][2][:, s:e] + factor * sum((contrib[j][2][:, s:e] for j in later), 0.0)
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("selected,factor", [((0, 2, 3), 2.0), ((1, 4), 2.0), ((0, 1, 2, 3, 4), 1.25), ((3,), 0.0)])
+def test_spaco_matches_the_hand_composition(selected, factor):
+    q, k, v, do = _layer(T=20, Hq=4, Hkv=2, d=4, B=2, seed=41)
+    scale = 0.6
+    o, lse, dq, dk, dv = oracle.sparse_chunked_layer(q, k, v, do, 4, scale, selected, factor)
+    edq, edk, edv = _spaco_expected(q, k, v, do, 4, scale, set(selected), factor)
+    o1, lse1, _ = oracle.dense_causal_attention(q, k, v, scale)
+    for a, b in ((o, o1), (lse, lse1), (dq, edq), (dk, edk), (dv, edv)):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+
+
+def test_spaco_with_every_chunk_and_no_compensation_is_exact():
+    """t = k with factor 1 is SeCO: the exact dense gradient."""
+    q, k, v, do = _layer(T=15, Hq=2, Hkv=1, d=4, seed=43)
+    got = oracle.sparse_chunked_layer(q, k, v, do, 4, 0.5, range(4), 1.0)
+    dq1, dk1, dv1 = oracle.dense_causal_attention_grad(q, k, v, do, 0.5)
+    for a, b in zip(got[2:], (dq1, dk1, dv1)):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+
+
+def test_spaco_pin_catches_a_compensated_direct_term():
+    """A plausible mistake -- scaling the chunk's own term along with the
+    relayed one -- fails the hand composition."""
+    q, k, v, do = _layer(T=12, Hq=2, Hkv=1, d=4, seed=47)
+    sel, f = (0, 2), 2.0
+    _, _, _, dk, _ = oracle.sparse_chunked_layer(q, k, v, do, 4, 0.7, sel, f)
+    _, edk, _ = _spaco_expected(q, k, v, do, 4, 0.7, set(sel), f)
+    do_0 = np.zeros_like(do)
+    do_0[:, 0:4] = do[:, 0:4]
+    own_0 = oracle.dense_causal_attention_grad(q, k, v, do_0, 0.7)[1]
+    bad = edk.copy()
+    bad[:, 0:4] += (f - 1.0) * own_0[:, 0:4]           # chunk 0's own term scaled too
+    assert np.abs(bad - dk).max() > 1e-3 and np.abs(edk - dk).max() < 1e-12
+
+
 # ---------------------------------------------------------------- input generator
 
 def test_inputs_are_seeded_and_block_addressable():
