@@ -84,8 +84,7 @@ typedef struct {
  *     q_len == 0 is a no-op.
  *   softmax_scale: finite, > 0 (usually 1/sqrt(d)).
  *   o (out), lse (out): overwritten.
- * BF16 requires d == 128 (else SEQATTN_ERR_UNSUPPORTED) and accepts any
- * q_start, q_len, prefix_len.  FP32 accepts any sizes and d in {64, 128}.
+ * Both dtypes accept any q_start, q_len, prefix_len and d in {64, 128}.
  */
 seqattn_status seqattn_chunk_fwd(const seqattn_problem* pb, int64_t q_start, int64_t q_len,
                                  int64_t prefix_len, float softmax_scale, const void* q,

@@ -51,30 +51,36 @@ namespace {
 
 constexpr int kBK = 128;   // keys per CTA
 constexpr int kBQ = 64;    // query rows per step
-constexpr int kD = 128;    // head dim
 constexpr int kComputeWarps = 8;                      // two per TMEM lane quadrant
 constexpr int kDQWarp0 = 2 + kComputeWarps;            // 4 dQ warps
 constexpr int kIssuerKV = kDQWarp0 + 4;                // dV, dK, dQ^T issuer
 constexpr int kIssuerDP = kIssuerKV + 1;               // dP^T issuer
 constexpr int kThreads = 32 * (kIssuerDP + 1);          // 16 warps
 
-constexpr int kKVTileBytes = kBK * kD * 2;         // 32 KB
-constexpr int kKVHalf = kKVTileBytes / 2;          // 16 KB: 128 rows x 128 B
-constexpr int kQTileBytes = kBQ * kD * 2;          // 16 KB
-constexpr int kQHalf = kQTileBytes / 2;            // 8 KB: 64 rows x 128 B
+constexpr int kDQRows = 128;                       // M of dQ^T = K^T dS^T (d rows, zero-padded when d = 64)
+constexpr int kKVHalf = kBK * 128;                 // 16 KB: one 64-column block of 128 rows x 128 B
+constexpr int kQHalf = kBQ * 128;                  // 8 KB: one 64-column block of 64 rows x 128 B
 constexpr int kPTileBytes = kBK * kBQ * 2;         // 16 KB: 128 keys x 64 q
-
-// shared memory carve-up (bytes from the 1024-aligned base)
-constexpr int kQStages = 3;                              // Q/dO/statistics ring depth
-constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + kKVTileBytes;
-constexpr int kOffQ = kOffV + kKVTileBytes;              // kQStages stages
-constexpr int kOffDO = kOffQ + kQStages * kQTileBytes;   // kQStages stages
-constexpr int kOffDS = kOffDO + kQStages * kQTileBytes;  // 2 buffers
-constexpr int kOffStat = kOffDS + 2 * kPTileBytes;       // kQStages x (-L log2 e [64], Delta [64])
+constexpr int kQStages = 3;                        // Q/dO/statistics ring depth
 constexpr int kStatBytes = 2 * kBQ * 4;
-constexpr int kSmemBytes = kOffStat + kQStages * kStatBytes;
-constexpr int kSmemAlloc = kSmemBytes + 1024;
+
+// Head-dim dependent sizes and the shared memory carve-up (bytes from the
+// 1024-aligned base).  The K tile always holds two 64-column blocks: with
+// d = 64 the second is zero, so that dQ^T = K^T dS^T keeps M = 128.
+template <int D>
+struct BwdCfg {
+  static constexpr int kKBytes = 2 * kKVHalf;                 // 32 KB
+  static constexpr int kVBytes = kBK * D * 2;                 // 32 KB or 16 KB
+  static constexpr int kQTileBytes = kBQ * D * 2;             // 16 KB or 8 KB
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kKBytes;
+  static constexpr int kOffQ = kOffV + kVBytes;               // kQStages stages
+  static constexpr int kOffDO = kOffQ + kQStages * kQTileBytes;   // kQStages stages
+  static constexpr int kOffDS = kOffDO + kQStages * kQTileBytes;  // 2 buffers
+  static constexpr int kOffStat = kOffDS + 2 * kPTileBytes;   // kQStages x (-L log2 e [64], Delta [64])
+  static constexpr int kSmemBytes = kOffStat + kQStages * kStatBytes;
+  static constexpr int kSmemAlloc = kSmemBytes + 1024;
+};
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColDK = 0;
@@ -138,10 +144,28 @@ __host__ __device__ constexpr uint32_t pair_col(int ks) {
 }
 constexpr uint32_t kDSPairs = 16;
 
+// P = 2^x with x = s scale log2(e) - L log2(e) for one thread's 32 scores,
+// as fp32 pairs (p2) and packed bf16 pairs (pk).
+__device__ __forceinline__ void form_p(const uint32_t (&r)[32], const uint64_t (&nl2)[16], uint64_t scale2,
+                                       uint64_t (&p2)[16], uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint64_t x = f2_fma(f2_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), scale2, nl2[j]);
+    float x0, x1;
+    f2_unpack(x, x0, x1);
+    const float p0 = ex2(x0), p1 = ex2(x1);
+    p2[j] = f2_pack(p0, p1);
+    pk[j] = pack_bf16x2(p0, p1);
+  }
+}
+
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_bf16_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                     const BwdParams p) {
+  using C = BwdCfg<D>;
+  constexpr int kDQWarps = D / 32;                   // dQ warps holding live d rows of dQ^T
   if (error_already_set(p.err)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -151,12 +175,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int abort_flag;
   Watchdog wd{&abort_flag, p.err};
 
-  // ---- work item: key tile kt (fastest), kv head g, batch b
+  // ---- work item: kv head g (fastest), key tile kt, batch b.  Key tiles of
+  // the prefix (the longest loops) start first and the shorter diagonal
+  // tiles fill the last wave.
   int idx = blockIdx.x;
-  const int kt = idx % p.n_ktiles;
-  idx /= p.n_ktiles;
   const int g = idx % p.Hkv;
-  const int b = idx / p.Hkv;
+  idx /= p.Hkv;
+  const int kt = idx % p.n_ktiles;
+  const int b = idx / p.n_ktiles;
   const int kb = p.kv_begin + kt * kBK;                  // absolute first key of the tile
   const int q_end = p.q_start + p.q_len;                 // one past the chunk's last row
   // first query tile that sees any key of this tile (the one holding row kb)
@@ -181,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.kv_done[i], 1);
       mbar_init(&bars.ds_empty[i], 1);
       mbar_init(&bars.dq_full[i], 1);
-      mbar_init(&bars.dq_empty[i], 4 * 32);
+      mbar_init(&bars.dq_empty[i], kDQWarps * 32);
     }
     for (int i = 0; i < 3; ++i) mbar_init(&bars.mma_final[i], 1);
     mbar_init(&bars.acc_done, 1);
@@ -191,16 +217,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&tmem_base_sh, kTmemCols);
     tmem_relinquish();
   }
+  if constexpr (D < 128) {
+    // second K block: the zero d rows 64..127 of the padded K^T operand of dQ^T
+    uint4* z = reinterpret_cast<uint4*>(smem + C::kOffK + kKVHalf);
+    for (int i = threadIdx.x; i < kKVHalf / 16; i += kThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
 
-  const uint32_t sK = smem_u32(smem + kOffK);
-  const uint32_t sV = smem_u32(smem + kOffV);
-  const uint32_t sQ = smem_u32(smem + kOffQ);
-  const uint32_t sDO = smem_u32(smem + kOffDO);
-  const uint32_t sDS = smem_u32(smem + kOffDS);
-  float* stat = reinterpret_cast<float*>(smem + kOffStat);  // [stage][-L log2 e 64 | Delta 64]
+  const uint32_t sK = smem_u32(smem + C::kOffK);
+  const uint32_t sV = smem_u32(smem + C::kOffV);
+  const uint32_t sQ = smem_u32(smem + C::kOffQ);
+  const uint32_t sDO = smem_u32(smem + C::kOffDO);
+  const uint32_t sDS = smem_u32(smem + C::kOffDS);
+  float* stat = reinterpret_cast<float*>(smem + C::kOffStat);  // [stage][-L log2 e 64 | Delta 64]
 
   auto step_head = [&](int n) { return g * p.G + n / nq; };
   auto step_qtile = [&](int n) { return qi_first + n % nq; };
@@ -213,11 +245,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&map_k);
       prefetch_tensormap(&map_v);
       const int krow = b * p.T + kb;
-      mbar_arrive_expect_tx(&bars.kv_full, 2 * kKVTileBytes);
-      tma_load_3d(smem + kOffK, &map_k, &bars.kv_full, 0, g, krow);
-      tma_load_3d(smem + kOffK + kKVHalf, &map_k, &bars.kv_full, 64, g, krow);
-      tma_load_3d(smem + kOffV, &map_v, &bars.kv_full, 0, g, krow);
-      tma_load_3d(smem + kOffV + kKVHalf, &map_v, &bars.kv_full, 64, g, krow);
+      mbar_arrive_expect_tx(&bars.kv_full, 2 * C::kVBytes);
+#pragma unroll
+      for (int blk = 0; blk < D / 64; ++blk) {
+        tma_load_3d(smem + C::kOffK + blk * kKVHalf, &map_k, &bars.kv_full, 64 * blk, g, krow);
+        tma_load_3d(smem + C::kOffV + blk * kKVHalf, &map_v, &bars.kv_full, 64 * blk, g, krow);
+      }
       int issued[kQStages] = {};
       for (int n = 0; n < n_steps; ++n) {
         const int st = n % kQStages;
@@ -227,11 +260,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wd.wait(&bars.q_empty[st], ph ^ 1)) break;
         const int qrow = b * p.q_len + qi * kBQ;
         const int64_t sblk = ((static_cast<int64_t>(b) * p.Hq + h) * p.n_q64 + qi) * (2 * kBQ);
-        mbar_arrive_expect_tx(&bars.q_full[st], 2 * kQTileBytes + kStatBytes);
-        tma_load_3d(smem + kOffQ + st * kQTileBytes, &map_q, &bars.q_full[st], 0, h, qrow);
-        tma_load_3d(smem + kOffQ + st * kQTileBytes + kQHalf, &map_q, &bars.q_full[st], 64, h, qrow);
-        tma_load_3d(smem + kOffDO + st * kQTileBytes, &map_do, &bars.q_full[st], 0, h, qrow);
-        tma_load_3d(smem + kOffDO + st * kQTileBytes + kQHalf, &map_do, &bars.q_full[st], 64, h, qrow);
+        mbar_arrive_expect_tx(&bars.q_full[st], 2 * C::kQTileBytes + kStatBytes);
+#pragma unroll
+        for (int blk = 0; blk < D / 64; ++blk) {
+          tma_load_3d(smem + C::kOffQ + st * C::kQTileBytes + blk * kQHalf, &map_q, &bars.q_full[st], 64 * blk, h,
+                      qrow);
+          tma_load_3d(smem + C::kOffDO + st * C::kQTileBytes + blk * kQHalf, &map_do, &bars.q_full[st], 64 * blk,
+                      h, qrow);
+        }
         bulk_load(stat + st * 2 * kBQ, p.stats + sblk, kStatBytes, &bars.q_full[st]);
         issued[st] = n + 1;
       }
@@ -245,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
       const uint32_t idesc_sdp = make_idesc_bf16(kBK, kBQ, false, false);  // M128 N64, K-major both
-      const uint32_t idesc_kv = make_idesc_bf16(kBK, kD, false, true);     // M128 N128, B MN-major
-      const uint32_t idesc_dq = make_idesc_bf16(kD, kBQ, true, true);      // M128 N64, both MN-major
+      const uint32_t idesc_kv = make_idesc_bf16(kBK, D, false, true);      // M128 N=d, B MN-major
+      const uint32_t idesc_dq = make_idesc_bf16(kDQRows, kBQ, true, true); // M128 N64, both MN-major
       // role 0: S^T (warp 1), role 1: dV, dK, dQ^T (kIssuerKV), role 2: dP^T
       const int role = warp == 1 ? 0 : (warp == kIssuerKV ? 1 : 2);
       bool ok = wd.wait(&bars.kv_full, 0);
@@ -265,10 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = wd.wait(&bars.q_full[st], (n / kQStages) & 1))) break;
           if (n >= 2 && !(ok = wd.wait(&release[bb], ((n - 2) >> 1) & 1))) break;
           tc_fence_after_sync();
-          const uint64_t bd = b_kmaj0 + static_cast<uint64_t>(st * (kQTileBytes >> 4));
+          const uint64_t bd = b_kmaj0 + static_cast<uint64_t>(st * (C::kQTileBytes >> 4));
           const uint32_t d = tmem + col_buf(bb) + off;
 #pragma unroll
-          for (int ks = 0; ks < kD / 16; ++ks)
+          for (int ks = 0; ks < D / 16; ++ks)
             umma_bf16_ss(d, a_kmaj + kmajor_off(kKVHalf, ks), bd + kmajor_off(kQHalf, ks), idesc_sdp,
                          ks > 0 ? 1u : 0u);
           umma_commit(&full[bb]);
@@ -287,14 +323,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t cb = tmem + col_buf(bb);
           if (!(ok = wd.wait(&bars.p_full[bb], (n >> 1) & 1))) break;
           tc_fence_after_sync();
-          const uint64_t dm = do_mn0 + static_cast<uint64_t>(st * (kQTileBytes >> 4));
+          const uint64_t dm = do_mn0 + static_cast<uint64_t>(st * (C::kQTileBytes >> 4));
 #pragma unroll
           for (int ks = 0; ks < kBQ / 16; ++ks)
             umma_bf16_ts(tmem + kColDV, cb + kOffS + pair_col(ks), dm + mnmajor_off(ks), idesc_kv,
                          (n > 0 || ks > 0) ? 1u : 0u);
           if (!(ok = wd.wait(&bars.ds_full[bb], (n >> 1) & 1))) break;
           tc_fence_after_sync();
-          const uint64_t qm = q_mn0 + static_cast<uint64_t>(st * (kQTileBytes >> 4));
+          const uint64_t qm = q_mn0 + static_cast<uint64_t>(st * (C::kQTileBytes >> 4));
 #pragma unroll
           for (int ks = 0; ks < kBQ / 16; ++ks)
             umma_bf16_ts(tmem + kColDK, cb + kOffS + pair_col(ks) + kDSPairs, qm + mnmajor_off(ks), idesc_kv,
@@ -352,18 +388,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // kept in fp32 for dS
       uint64_t p2[16];
       uint32_t pk[16];                                  // packed bf16 pairs
+      form_p(r, nl2, scale2, p2, pk);
+      if (masked) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint64_t x = f2_fma(f2_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), scale2, nl2[j]);
-        float x0, x1;
-        f2_unpack(x, x0, x1);
-        float p0 = ex2(x0), p1 = ex2(x1);
-        if (masked) {
+        for (int j = 0; j < 16; ++j) {
+          float p0, p1;
+          f2_unpack(p2[j], p0, p1);
           if (key > q_abs0 + 2 * j) p0 = 0.f;
           if (key > q_abs0 + 2 * j + 1) p1 = 0.f;
+          p2[j] = f2_pack(p0, p1);
+          pk[j] = pack_bf16x2(p0, p1);
         }
-        p2[j] = f2_pack(p0, p1);
-        pk[j] = pack_bf16x2(p0, p1);
       }
       // P^T pairs over the first 16 of this warp's S^T columns: dV can start
       tmem_st16(cb + kOffS + c_off, pk);
@@ -412,11 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const bool store = key < q_end;                   // keys of a partial last tile past the chunk are dropped
       const int64_t row = (static_cast<int64_t>(b) * p.T + key) * p.Hkv + g;
-      float4* dst = reinterpret_cast<float4*>((half == 0 ? p.dk : p.dv) + row * kD);
+      float4* dst = reinterpret_cast<float4*>((half == 0 ? p.dk : p.dv) + row * D);
       const uint32_t col = half == 0 ? kColDK : kColDV;
       const float f = half == 0 ? p.scale : 1.f;
 #pragma unroll
-      for (int c0 = 0; c0 < kD; c0 += 64) {
+      for (int c0 = 0; c0 < D; c0 += 64) {
         uint32_t r0[32], r1[32];
         tmem_ld32(tmem + lane_base + col + c0, r0);
         tmem_ld32(tmem + lane_base + col + c0 + 32, r1);
@@ -446,7 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int dcol = quad * 32 + lane;                  // head-dim column (TMEM lane)
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    for (int n = 0; n < n_steps; ++n) {
+    // with d = 64 the lanes 64..127 of dQ^T are the zero padding: no work
+    for (int n = 0; quad < kDQWarps && n < n_steps; ++n) {
       const int bb = n & 1;
       if (!warp_wait(wd, &bars.dq_full[bb], (n >> 1) & 1)) break;
       tc_fence_after_sync();
@@ -458,8 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bars.dq_empty[bb]);
       const int h = step_head(n);
       const int qi = step_qtile(n);
-      float* base = p.dq + ((static_cast<int64_t>(b) * p.q_len + qi * kBQ) * p.Hq + h) * kD + dcol;
-      const int64_t rstride = static_cast<int64_t>(p.Hq) * kD;
+      float* base = p.dq + ((static_cast<int64_t>(b) * p.q_len + qi * kBQ) * p.Hq + h) * D + dcol;
+      const int64_t rstride = static_cast<int64_t>(p.Hq) * D;
       const int rows = p.q_len - qi * kBQ;              // rows of this query tile inside the chunk
       if (rows >= kBQ) {
         // full tile: 64 back-to-back reductions (a per-row predicate here
@@ -488,13 +524,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <int D>
+cudaError_t launch_bwd_bf16_d(const BwdParams& p, const Bf16BwdMaps& maps, unsigned grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(bwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       BwdCfg<D>::kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  bwd_bf16_kernel<D><<<grid, kThreads, BwdCfg<D>::kSmemAlloc, s>>>(maps.q, maps.k, maps.v, maps.d_o, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_bf16(const ChunkGeom& g, const Bf16BwdMaps& maps, const float* stats,
                             float* dq, float* dk, float* dv, unsigned int* err, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(bwd_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemAlloc);
-  if (e != cudaSuccess) return e;
   BwdParams p;
   p.B = g.B;
   p.Hq = g.Hq;
@@ -514,8 +556,7 @@ cudaError_t launch_bwd_bf16(const ChunkGeom& g, const Bf16BwdMaps& maps, const f
   p.dv = dv;
   p.err = err;
   const unsigned grid = static_cast<unsigned>(p.n_ktiles) * g.Hkv * g.B;
-  bwd_bf16_kernel<<<grid, kThreads, kSmemAlloc, s>>>(maps.q, maps.k, maps.v, maps.d_o, p);
-  return cudaGetLastError();
+  return g.d == 64 ? launch_bwd_bf16_d<64>(p, maps, grid, s) : launch_bwd_bf16_d<128>(p, maps, grid, s);
 }
 
 }  // namespace seqattn

@@ -38,21 +38,25 @@ namespace {
 
 constexpr int kBM = 128;                    // query rows per CTA
 constexpr int kBN = 128;                    // keys per tile
-constexpr int kD = 128;                     // head dim
-constexpr int kTileBytes = kBM * kD * 2;    // 32 KB: one 128x128 bf16 tile
-constexpr int kHalfBytes = kTileBytes / 2;  // one 64-column (128-byte) block
+constexpr int kBlockBytes = kBM * 128;      // one 64-column (128-byte) block of a 128-row tile
 constexpr int kSoftmaxWarps = 8;
 constexpr int kVWarp = 2 + kSoftmaxWarps;           // V producer warp
 constexpr int kPVWarp = kVWarp + 1;                 // second MMA issuer (PV)
 constexpr int kThreads = 32 * (kPVWarp + 1);        // 12 warps
 constexpr int kStages = 3;                          // K and V ring depth
 
-// shared memory carve-up (bytes from the 1024-aligned base)
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;              // kStages stages
-constexpr int kOffV = kOffK + kStages * kTileBytes;    // kStages stages
-constexpr int kSmemBytes = kOffV + kStages * kTileBytes;
-constexpr int kSmemAlloc = kSmemBytes + 1024;    // + alignment slack
+// Head-dim dependent sizes: a 128-row tile of D bf16 columns is D/64 blocks
+// of 128 rows x 128 B, and the shared memory carve-up (bytes from the
+// 1024-aligned base).
+template <int D>
+struct FwdCfg {
+  static constexpr int kTileBytes = kBM * D * 2;    // 32 KB (D = 128) or 16 KB (D = 64)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kTileBytes;              // kStages stages
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;    // kStages stages
+  static constexpr int kSmemBytes = kOffV + kStages * kTileBytes;
+  static constexpr int kSmemAlloc = kSmemBytes + 1024;          // + alignment slack
+};
 
 // TMEM columns: S buffers at 0 and 128, O_0 at 256, O_1 at 384.  P of key
 // half h (bf16 pairs, 32 columns) overwrites columns [64h, 64h + 32) of its S
@@ -97,19 +101,22 @@ __device__ __forceinline__ bool warp_wait(Watchdog& wd, uint64_t* bar, uint32_t 
 // the 14-bit start-address field (16-byte units), so each MMA's operands are
 // the base plus a compile-time constant -- building the full descriptor in
 // front of every MMA would put a serial integer chain on the issuing thread.
-// K-major 128x128 bf16 tile = two 64-column blocks of 128 rows x 128 B;
+// K-major 128-row bf16 tile = 64-column blocks of 128 rows x 128 B;
 // K-step ks (16 elements) -> block ks/4, byte offset 32*(ks%4) in the row.
 __host__ __device__ constexpr uint32_t kmajor_off(int ks) {
-  return static_cast<uint32_t>(((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4);
+  return static_cast<uint32_t>(((ks >> 2) * kBlockBytes + (ks & 3) * 32) >> 4);
 }
-// V tile [128 keys][128 d] as the MN-major B operand (N = d, K = keys):
-// 8-key groups of 1024 B along K, the two 64-wide d blocks 16 KB apart.
+// V tile [128 keys][D] as the MN-major B operand (N = d, K = keys):
+// 8-key groups of 1024 B along K, the 64-wide d blocks 16 KB apart.
 __host__ __device__ constexpr uint32_t vmn_off(int ks) { return static_cast<uint32_t>((ks * 2048) >> 4); }
-constexpr uint32_t kTileUnits = kTileBytes >> 4;
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
+  using C = FwdCfg<D>;
+  constexpr int kTileBytes = C::kTileBytes;
+  constexpr uint32_t kTileUnits = kTileBytes >> 4;
   if (error_already_set(p.err)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -162,9 +169,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
 
-  const uint32_t sQ = smem_u32(smem + kOffQ);
-  const uint32_t sK = smem_u32(smem + kOffK);
-  const uint32_t sV = smem_u32(smem + kOffV);
+  const uint32_t sQ = smem_u32(smem + C::kOffQ);
+  const uint32_t sK = smem_u32(smem + C::kOffK);
+  const uint32_t sV = smem_u32(smem + C::kOffV);
 
   if (warp == 0 || warp == kVWarp) {
     // ------------------------------------------------------------ producers
@@ -173,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const bool is_k = (warp == 0);
       const CUtensorMap* map = is_k ? &map_k : &map_v;
-      const int off = is_k ? kOffK : kOffV;
+      const int off = is_k ? C::kOffK : C::kOffV;
       uint64_t* full = is_k ? bars.k_full : bars.v_full;
       uint64_t* empty = is_k ? bars.k_empty : bars.v_empty;
       prefetch_tensormap(map);
@@ -181,8 +188,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&map_q);
         const int qrow = b * p.q_len + qt * kBM;
         mbar_arrive_expect_tx(&bars.q_full, kTileBytes);
-        tma_load_3d(smem + kOffQ, &map_q, &bars.q_full, 0, h, qrow);
-        tma_load_3d(smem + kOffQ + kHalfBytes, &map_q, &bars.q_full, 64, h, qrow);
+#pragma unroll
+        for (int blk = 0; blk < D / 64; ++blk)
+          tma_load_3d(smem + C::kOffQ + blk * kBlockBytes, &map_q, &bars.q_full, 64 * blk, h, qrow);
       }
       int issued[kStages] = {};
       for (int t = 0; t < n_kv; ++t) {
@@ -191,8 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int krow = b * p.T + p.kv_begin + t * kBN;
         if (!wd.wait(&empty[st], ph ^ 1)) break;
         mbar_arrive_expect_tx(&full[st], kTileBytes);
-        tma_load_3d(smem + off + st * kTileBytes, map, &full[st], 0, g, krow);
-        tma_load_3d(smem + off + st * kTileBytes + kHalfBytes, map, &full[st], 64, g, krow);
+#pragma unroll
+        for (int blk = 0; blk < D / 64; ++blk)
+          tma_load_3d(smem + off + st * kTileBytes + blk * kBlockBytes, map, &full[st], 64 * blk, g, krow);
         issued[st] = t + 1;
       }
       if (wd.aborted()) {
@@ -209,10 +218,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // overwrites P(t-2), so S(t) waits for PV(t-2) to complete.
     if (lane == 0) {
       const uint32_t idesc_s = make_idesc_bf16(kBM, kBN, false, false);
-      const uint32_t idesc_o = make_idesc_bf16(kBM, kD, false, true);
+      const uint32_t idesc_o = make_idesc_bf16(kBM, D, false, true);
       const uint64_t q_desc = make_desc_sw128(sQ, 16, 1024);
       const uint64_t k_desc0 = make_desc_sw128(sK, 16, 1024);
-      const uint64_t v_desc0 = make_desc_sw128(sV, kHalfBytes, 1024);
+      const uint64_t v_desc0 = make_desc_sw128(sV, kBlockBytes, 1024);
       const int me = (warp == 1) ? 0 : 1;
       bool ok = true;
       if (me == 0) {
@@ -224,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after_sync();
           const uint64_t kd = k_desc0 + static_cast<uint64_t>(ks_st * kTileUnits);
 #pragma unroll
-          for (int ks = 0; ks < kD / 16; ++ks)
+          for (int ks = 0; ks < D / 16; ++ks)
             umma_bf16_ss(tmem + kColS + (t & 1) * kBN, q_desc + kmajor_off(ks), kd + kmajor_off(ks), idesc_s,
                          ks > 0 ? 1u : 0u);
           umma_commit(&bars.s_full[t & 1]);
@@ -307,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = warp_wait(wd, &bars.pv_done[u & 1], (u >> 1) & 1))) break;
           tc_fence_after_sync();
 #pragma unroll
-          for (int c0 = 0; c0 < kD; c0 += 64) {
+          for (int c0 = 0; c0 < D; c0 += 64) {
             uint32_t r0[32], r1[32];
             tmem_ld32(colO + c0, r0);
             tmem_ld32(colO + c0 + 32, r1);
@@ -356,8 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- epilogue: merge the two halves of every row.  The exchange uses the
     // K ring, idle once the last PV product has completed.
-    float (*merge_m)[kBM] = reinterpret_cast<float (*)[kBM]>(smem + kOffK);
-    float (*merge_l)[kBM] = reinterpret_cast<float (*)[kBM]>(smem + kOffK + 2 * kBM * 4);
+    float (*merge_m)[kBM] = reinterpret_cast<float (*)[kBM]>(smem + C::kOffK);
+    float (*merge_l)[kBM] = reinterpret_cast<float (*)[kBM]>(smem + C::kOffK + 2 * kBM * 4);
     merge_m[half][row] = m_run;
     merge_l[half][row] = l_run;
     named_barrier_sync(1, kSoftmaxWarps * 32);
@@ -372,14 +381,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float L = merge_l[0][row] * a0 + merge_l[1][row] * a1;
       const float inv = 1.f / L;
       const float f0 = a0 * inv, f1 = a1 * inv;
-      // this warp writes head-dim columns [64 half, 64 half + 64) of the row
-      uint4* orow = reinterpret_cast<uint4*>(p.o + ((static_cast<int64_t>(b) * p.q_len + qrow) * p.Hq + h) * kD +
-                                             half * 64);
+      // this warp writes head-dim columns [D/2 half, D/2 half + D/2) of the row
+      uint4* orow = reinterpret_cast<uint4*>(p.o + ((static_cast<int64_t>(b) * p.q_len + qrow) * p.Hq + h) * D +
+                                             half * (D / 2));
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
         uint32_t r0[32], r1[32];
-        tmem_ld32(tmem + lane_base + kColO + half * 64 + c0, r0);
-        tmem_ld32(tmem + lane_base + kColO + 128 + half * 64 + c0, r1);
+        tmem_ld32(tmem + lane_base + kColO + half * (D / 2) + c0, r0);
+        tmem_ld32(tmem + lane_base + kColO + 128 + half * (D / 2) + c0, r1);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; j += 8) {
@@ -408,13 +417,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <int D>
+cudaError_t launch_fwd_bf16_d(const FwdParams& p, const Bf16FwdMaps& maps, unsigned grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       FwdCfg<D>::kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  fwd_bf16_kernel<D><<<grid, kThreads, FwdCfg<D>::kSmemAlloc, s>>>(maps.q, maps.k, maps.v, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const ChunkGeom& g, const Bf16FwdMaps& maps, void* o, float* lse,
                             unsigned int* err, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemAlloc);
-  if (e != cudaSuccess) return e;
   FwdParams p;
   p.B = g.B;
   p.Hq = g.Hq;
@@ -430,8 +445,7 @@ cudaError_t launch_fwd_bf16(const ChunkGeom& g, const Bf16FwdMaps& maps, void* o
   p.lse = lse;
   p.err = err;
   const unsigned grid = static_cast<unsigned>(p.n_qtiles) * g.Hq * g.B;
-  fwd_bf16_kernel<<<grid, kThreads, kSmemAlloc, s>>>(maps.q, maps.k, maps.v, p);
-  return cudaGetLastError();
+  return g.d == 64 ? launch_fwd_bf16_d<64>(p, maps, grid, s) : launch_fwd_bf16_d<128>(p, maps, grid, s);
 }
 
 }  // namespace seqattn

@@ -128,10 +128,6 @@ seqattn_status check_chunk(const seqattn_problem* pb, int64_t q_start, int64_t q
     return fail(SEQATTN_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
   if (static_cast<int64_t>(pb->batch) * q_len > INT32_MAX)
     return fail(SEQATTN_ERR_INVALID_ARG, "batch * q_len exceeds 2^31 - 1 rows");
-  if (pb->dtype == SEQATTN_BF16) {
-    if (pb->head_dim != 128)
-      return fail(SEQATTN_ERR_UNSUPPORTED, "bf16 path needs head_dim 128 (got %d)", pb->head_dim);
-  }
   g->B = pb->batch;
   g->Hq = pb->num_q_heads;
   g->Hkv = pb->num_kv_heads;

@@ -291,6 +291,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -315,6 +326,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -330,29 +348,6 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// 2^x on the FMA/ALU pipes (so part of a softmax tile can bypass the MUFU
-// unit).  Cody-Waite style split x = n + f with n = round(x) taken from the
-// mantissa of x + 1.5*2^23 and f in [-1/2, 1/2]; 2^f by a cubic whose
-// coefficients were fitted for this file (iteratively reweighted least
-// squares on the relative error over [-1/2, 1/2]; max relative error
-// 7.5e-5, far below the 2^-9 rounding of the bf16 P it feeds); 2^n added to
-// the exponent field.  x is clamped to >= -125 so the result stays a normal
-// float (2^-125 is negligible next to a softmax row sum >= 1).
-constexpr float kEx2C0 = 0.99992806f;
-constexpr float kEx2C1 = 0.69326103f;
-constexpr float kEx2C2 = 0.24261114f;
-constexpr float kEx2C3 = 0.05517161f;
-
-__device__ __forceinline__ float ex2_poly(float x) {
-  x = fmaxf(x, -125.f);
-  const float t = x + 12582912.f;
-  const float f = x - (t - 12582912.f);
-  float p = fmaf(kEx2C3, f, kEx2C2);
-  p = fmaf(p, f, kEx2C1);
-  p = fmaf(p, f, kEx2C0);
-  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
 }
 
 // Two floats -> packed bf16x2 (round to nearest even); `lo` in the low half.

@@ -77,7 +77,6 @@ def _fwd(lib, pb, q_start=0, q_len=128, prefix=0, scale=0.088, ptrs=None):
     (dict(head_dim=96), 1),              # unsupported head_dim
     (dict(batch=0), 1),
     (dict(dtype=7), 1),
-    (dict(head_dim=64), 2),              # bf16 path needs d=128
 ])
 def test_problem_validation(lib, kw, code):
     st, msg = _fwd(lib, _pb(**kw))

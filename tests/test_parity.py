@@ -195,6 +195,8 @@ def _check_bf16_layer(B, T, Hq, Hkv, d, chunk, seed):
     (1, 384, 2, 1, 128, 160),    # chunk starts off the 64/128 grid
     (1, 200, 2, 2, 128, 200),    # one chunk (D=1) of 200 rows, MHA
     (1, 70, 2, 1, 128, 1),       # one-row chunks
+    (1, 768, 4, 2, 64, 256),     # head_dim 64, on the tile grid
+    (2, 300, 4, 1, 64, 100),     # head_dim 64, ragged, G=4, batch 2
 ])
 def test_bf16_ragged_shapes(B, T, Hq, Hkv, d, chunk):
     _check_bf16_layer(B, T, Hq, Hkv, d, chunk, seed=12)
