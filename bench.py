@@ -33,7 +33,7 @@ FALLBACK_SUSTAINED_TFLOPS = 1700.0   # used only when no measured peaks file exi
 # DRAM traffic (bytes read + written) per backward launch, from the ncu
 # launch list of the bench workload (average over its 16 chunk launches);
 # set to None whenever the kernel changes until it is measured again.
-BWD_TRAFFIC_BYTES_PER_LAUNCH = 401.3e6   # bwd_bf16_kernel with double-buffered step buffers
+BWD_TRAFFIC_BYTES_PER_LAUNCH = None   # bwd_bf16_kernel grid order changed: not yet measured
 
 
 def parse_args():

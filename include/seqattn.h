@@ -147,6 +147,25 @@ seqattn_status seqattn_chunk_bwd_noalloc(const seqattn_problem* pb, int64_t q_st
 seqattn_status seqattn_reset_accum(const seqattn_problem* pb, float* dk_accum, float* dv_accum,
                                    seqattn_stream_t stream);
 
+/*
+ * Multiply rows [row_begin, row_end) of both float32 accumulators by `scale`;
+ * scale == 0 stores zeros.  This is the step SpaCO adds to the chunk loop
+ * (SeCO review page, "Referee Report": the Summary, where t of the k chunks
+ * are backpropagated and the relayed KV-cache gradient is multiplied by k/t,
+ * and the major comments on Algorithm 2 and Section 6.4, where the factor
+ * is capped at 2).  Before a selected chunk's backward, its own rows --
+ * which then hold only what later chunks relayed into them -- are scaled by
+ * the compensation factor; the rows of a chunk that is not selected are
+ * zeroed, since nothing propagates from them.
+ *   0 <= row_begin <= row_end <= seq_capacity; scale finite.  Every batch
+ *   entry and every key/value head of those rows is scaled.  dk_accum,
+ *   dv_accum: [B, seq_capacity, Hkv, d] float32, 16-byte aligned.
+ * Async on `stream`; INVALID_ARG before any launch on a bad argument.
+ */
+seqattn_status seqattn_scale_accum_rows(const seqattn_problem* pb, int64_t row_begin,
+                                        int64_t row_end, float scale, float* dk_accum,
+                                        float* dv_accum, seqattn_stream_t stream);
+
 /* Bytes of workspace seqattn_chunk_bwd needs for a chunk of q_len rows
  * (0 for an invalid problem).  Pure host function. */
 size_t seqattn_bwd_workspace_size(const seqattn_problem* pb, int64_t q_len);

@@ -27,6 +27,7 @@ EXPORTED = (
     "seqattn_chunk_bwd",
     "seqattn_chunk_bwd_noalloc",
     "seqattn_reset_accum",
+    "seqattn_scale_accum_rows",
     "seqattn_bwd_workspace_size",
     "seqattn_sync_status",
     "seqattn_status_string",
@@ -75,6 +76,8 @@ def load_library(path=LIB_PATH):
     lib.seqattn_chunk_bwd_noalloc.restype = ctypes.c_int
     lib.seqattn_reset_accum.argtypes = [P, vp, vp, vp]
     lib.seqattn_reset_accum.restype = ctypes.c_int
+    lib.seqattn_scale_accum_rows.argtypes = [P, i64, i64, f32, vp, vp, vp]
+    lib.seqattn_scale_accum_rows.restype = ctypes.c_int
     lib.seqattn_bwd_workspace_size.argtypes = [P, i64]
     lib.seqattn_bwd_workspace_size.restype = sz
     lib.seqattn_sync_status.argtypes = [vp]
@@ -181,6 +184,18 @@ def reset_accum(dk_accum, dv_accum, num_q_heads=None, stream=None):
                                               _stream(stream)))
 
 
+def scale_accum_rows(dk_accum, dv_accum, row_begin, row_end, scale, stream=None):
+    """Multiply rows [row_begin, row_end) of two float32 [B, T, H, d] arrays
+    (the running sums, or any such pair; the same tensor may be passed twice)
+    by ``scale`` (0 stores zeros)."""
+    _need(dk_accum, "dk_accum", torch.float32)
+    _need(dv_accum, "dv_accum", torch.float32, dk_accum.shape)
+    B, T, H, d = dk_accum.shape
+    pb = Problem(B, H, H, d, T, SEQATTN_FP32)
+    _check(load_library().seqattn_scale_accum_rows(ctypes.byref(pb), row_begin, row_end, scale,
+                                                   _ptr(dk_accum), _ptr(dv_accum), _stream(stream)))
+
+
 def sync_status(stream=None):
     """Synchronise the stream and raise if a kernel gave up a bounded wait."""
     _check(load_library().seqattn_sync_status(_stream(stream)))
@@ -242,6 +257,57 @@ def layer_forward_backward(q, k, v, d_o, chunk, scale=None, bufs=None, stream=No
     for i, s in order:
         e = min(s + chunk, T)
         dq_c = bufs.dq[:, s:e]
+        tgt = dq_c if dq_c.is_contiguous() else torch.empty_like(dq_c.contiguous())
+        chunk_bwd(_rows(q, s, e), k, v, _rows(bufs.o, s, e), bufs.lse_chunks[i], _rows(d_o, s, e),
+                  tgt, bufs.dk, bufs.dv, s, s, scale, bufs.workspace, stream)
+        if tgt is not dq_c:
+            dq_c.copy_(tgt)
+    return bufs
+
+
+def spaco_factor(num_chunks, num_selected, cap=2.0):
+    """SpaCO's compensation factor for t = num_selected of k = num_chunks
+    chunks: k / t, capped (at 2 in the deployed method)."""
+    return min(num_chunks / num_selected, cap)
+
+
+def spaco_layer_forward_backward(q, k, v, d_o, chunk, selected, factor=None, scale=None, bufs=None,
+                                 stream=None):
+    """One SpaCO pass of the chunked layer: reset the running sums, forward
+    every chunk (the inference pass that builds the caches), then visit the
+    chunks last to first.  A selected chunk scales the cache gradient relayed
+    into its own rows by ``factor`` and runs its backward; a chunk that is not
+    selected has its rows zeroed and no backward.  ``selected`` holds the
+    sampled chunk indices (drawn by the caller); ``factor`` defaults to
+    ``spaco_factor(D, len(selected))``.  dQ rows of unselected chunks are
+    zero.  Returns the LayerBuffers."""
+    B, T, Hq, d = q.shape
+    if bufs is None:
+        bufs = LayerBuffers(q, k, chunk)
+    chosen = set(int(i) for i in selected)
+    n_chunks = len(bufs.starts)
+    if not chosen or min(chosen) < 0 or max(chosen) >= n_chunks:
+        raise ValueError(f"selected chunk indices must lie in [0, {n_chunks})")
+    if factor is None:
+        factor = spaco_factor(n_chunks, len(chosen))
+    reset_accum(bufs.dk, bufs.dv, Hq, stream)
+    for i, s in enumerate(bufs.starts):
+        e = min(s + chunk, T)
+        o_c = bufs.o[:, s:e]
+        if o_c.is_contiguous():
+            chunk_fwd(_rows(q, s, e), k, v, o_c, bufs.lse_chunks[i], s, s, scale, stream)
+        else:
+            tmp = torch.empty_like(o_c.contiguous())
+            chunk_fwd(_rows(q, s, e), k, v, tmp, bufs.lse_chunks[i], s, s, scale, stream)
+            o_c.copy_(tmp)
+    for i, s in reversed(list(enumerate(bufs.starts))):
+        e = min(s + chunk, T)
+        dq_c = bufs.dq[:, s:e]
+        if i not in chosen:
+            scale_accum_rows(bufs.dk, bufs.dv, s, e, 0.0, stream)
+            scale_accum_rows(bufs.dq, bufs.dq, s, e, 0.0, stream)   # no dQ for this chunk
+            continue
+        scale_accum_rows(bufs.dk, bufs.dv, s, e, factor, stream)
         tgt = dq_c if dq_c.is_contiguous() else torch.empty_like(dq_c.contiguous())
         chunk_bwd(_rows(q, s, e), k, v, _rows(bufs.o, s, e), bufs.lse_chunks[i], _rows(d_o, s, e),
                   tgt, bufs.dk, bufs.dv, s, s, scale, bufs.workspace, stream)

@@ -36,6 +36,9 @@ cudaError_t launch_bwd_prep_f32(const ChunkGeom& g, const float* o, const float*
 
 // ---- zero fill of the float32 accumulators ---------------------------------
 cudaError_t launch_zero_f32(float* a, float* b, int64_t n, cudaStream_t s);
+// rows [r0, r1) of two [B, T, row_floats] float32 arrays times `scale` (0 stores zeros)
+cudaError_t launch_scale_rows_f32(float* a, float* b, int B, int64_t T, int64_t r0, int64_t r1,
+                                  int64_t row_floats, float scale, cudaStream_t s);
 
 // ---- bf16 tensor-core path (TMA + tcgen05 + TMEM) -------------------------
 // Tensor maps are built by the front end (see tma_maps in seqattn_api.cu).

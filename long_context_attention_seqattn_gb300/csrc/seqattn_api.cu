@@ -247,6 +247,23 @@ seqattn_status seqattn_reset_accum(const seqattn_problem* pb, float* dk_accum, f
   return e == cudaSuccess ? ok() : cuda_fail(e, "reset launch");
 }
 
+seqattn_status seqattn_scale_accum_rows(const seqattn_problem* pb, int64_t row_begin,
+                                        int64_t row_end, float scale, float* dk_accum,
+                                        float* dv_accum, seqattn_stream_t stream) {
+  seqattn_status s = check_problem(pb);
+  if (s != SEQATTN_OK) return s;
+  if (row_begin < 0 || row_end < row_begin || row_end > pb->seq_capacity)
+    return fail(SEQATTN_ERR_INVALID_ARG, "need 0 <= row_begin <= row_end <= seq_capacity (got %lld, %lld)",
+                (long long)row_begin, (long long)row_end);
+  if (!isfinite(scale)) return fail(SEQATTN_ERR_INVALID_ARG, "scale must be finite");
+  s = check_ptrs({{dk_accum, "dk_accum"}, {dv_accum, "dv_accum"}});
+  if (s != SEQATTN_OK) return s;
+  cudaError_t e = launch_scale_rows_f32(dk_accum, dv_accum, pb->batch, pb->seq_capacity, row_begin, row_end,
+                                        static_cast<int64_t>(pb->num_kv_heads) * pb->head_dim, scale,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "scale launch");
+}
+
 size_t seqattn_bwd_workspace_size(const seqattn_problem* pb, int64_t q_len) {
   if (check_problem(pb) != SEQATTN_OK || q_len < 0) return 0;
   return workspace_bytes(pb, q_len);

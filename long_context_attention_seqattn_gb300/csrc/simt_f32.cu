@@ -339,6 +339,28 @@ __global__ void zero2_kernel(float4* __restrict__ a, float4* __restrict__ b, int
   }
 }
 
+// rows [r0, r0 + n_rows) of two [B, T, row4] float4 arrays times `scale`
+// (0 stores zeros, so NaN or Inf there is cleared too); grid-stride.
+__global__ void scale2_rows_kernel(float4* __restrict__ a, float4* __restrict__ b, int64_t T, int64_t r0,
+                                   int64_t n_rows, int64_t row4, int64_t n4, float scale) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t per_batch = n_rows * row4;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const int64_t bi = i / per_batch;
+    const int64_t j = (bi * T + r0) * row4 + (i - bi * per_batch);
+    if (scale == 0.f) {
+      a[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      b[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      float4 x = a[j], y = b[j];
+      x.x *= scale; x.y *= scale; x.z *= scale; x.w *= scale;
+      y.x *= scale; y.y *= scale; y.z *= scale; y.w *= scale;
+      a[j] = x;
+      b[j] = y;
+    }
+  }
+}
+
 int num_sms() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -427,6 +449,20 @@ cudaError_t launch_bwd_stats_bf16(const ChunkGeom& g, const void* o, const void*
 cudaError_t launch_bwd_prep_f32(const ChunkGeom& g, const float* o, const float* d_o, float* delta,
                                 cudaStream_t s) {
   return prep<float>(g, o, d_o, delta, nullptr, s);
+}
+
+cudaError_t launch_scale_rows_f32(float* a, float* b, int B, int64_t T, int64_t r0, int64_t r1,
+                                  int64_t row_floats, float scale, cudaStream_t s) {
+  const int64_t row4 = row_floats / 4;
+  const int64_t n4 = static_cast<int64_t>(B) * (r1 - r0) * row4;
+  if (n4 == 0) return cudaSuccess;
+  const int threads = 256;
+  int64_t blocks = (n4 + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  if (blocks > cap) blocks = cap;
+  scale2_rows_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
+      reinterpret_cast<float4*>(a), reinterpret_cast<float4*>(b), T, r0, r1 - r0, row4, n4, scale);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_zero_f32(float* a, float* b, int64_t n, cudaStream_t s) {

@@ -96,6 +96,21 @@ def test_chunk_validation(lib):
     assert st == 1 and "aligned" in msg
 
 
+def test_scale_rows_validation(lib):
+    """Argument checks of seqattn_scale_accum_rows, all refused before any launch."""
+    pb = _pb()
+    f = lib.seqattn_scale_accum_rows
+    assert f(ctypes.byref(pb), 0, 1025, 2.0, P, P, NUL) == 1          # past seq_capacity
+    assert f(ctypes.byref(pb), 10, 9, 2.0, P, P, NUL) == 1            # row_end < row_begin
+    assert f(ctypes.byref(pb), -1, 4, 2.0, P, P, NUL) == 1
+    assert f(ctypes.byref(pb), 0, 4, float("nan"), P, P, NUL) == 1
+    assert f(ctypes.byref(pb), 0, 4, float("inf"), P, P, NUL) == 1
+    assert f(ctypes.byref(pb), 0, 4, 2.0, NUL, P, NUL) == 1
+    st = f(ctypes.byref(pb), 0, 4, 2.0, P, MIS, NUL)
+    assert st == 1 and b"aligned" in lib.seqattn_last_error()
+    assert f(None, 0, 4, 2.0, P, P, NUL) == 1
+
+
 def test_empty_chunk_is_ok_without_touching_memory(lib):
     assert _fwd(lib, _pb(), q_len=0, ptrs=[NUL] * 5)[0] == 0
     st = lib.seqattn_chunk_bwd(ctypes.byref(_pb()), 0, 0, 0, 0.1, *([NUL] * 10), 0, NUL)

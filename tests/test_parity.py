@@ -265,6 +265,34 @@ def test_bf16_ragged_guard_bands_untouched():
     assert float(dk[:, qs + c:].abs().max()) == 0.0 and float(dv[:, qs + c:].abs().max()) == 0.0
 
 
+@pytest.mark.parametrize("dtype,B,T,Hq,Hkv,d,chunk,selected,factor", [
+    ("bf16", 1, 1024, 4, 2, 128, 128, (0, 3, 5, 6), None),    # k/t = 2
+    ("bf16", 2, 700, 4, 1, 64, 100, (1, 6), None),            # ragged last chunk, cap at 2
+    ("bf16", 1, 512, 2, 2, 128, 128, (0, 1, 2, 3), 1.0),      # every chunk: the exact pass
+    ("fp32", 1, 300, 4, 2, 64, 64, (0, 2, 4), 1.5),
+])
+def test_spaco_pass_matches_oracle(dtype, B, T, Hq, Hkv, d, chunk, selected, factor):
+    """SpaCO through the library: forward over every chunk, backward over the
+    selected chunks with the relayed rows compensated, other chunks' rows
+    zeroed (the float64 oracle's sparse_chunked_layer on the same inputs)."""
+    cpu = small_inputs(B, T, Hq, Hkv, d, dtype, 77)
+    n_chunks = -(-T // chunk)
+    f = binding.spaco_factor(n_chunks, len(selected)) if factor is None else factor
+    bufs = binding.spaco_layer_forward_backward(*[x.cuda() for x in cpu], chunk, selected, f)
+    binding.sync_status()
+    ref = oracle.sparse_chunked_layer(*(x.to(torch.float64).numpy() for x in cpu), chunk, d ** -0.5,
+                                      selected, f)
+    got = (bufs.o, binding.gather_lse(bufs), bufs.dq, bufs.dk, bufs.dv)
+    check = assert_bf16 if dtype == "bf16" else assert_f32
+    for name, a, r in zip(("O", "LSE", "dQ", "dK", "dV"), got, ref):
+        check(f"SpaCO {name}", cpu64(a), r)
+    # rows of chunks that were not selected carry nothing
+    for i in set(range(n_chunks)) - set(selected):
+        s, e = i * chunk, min((i + 1) * chunk, T)
+        for t in (bufs.dq, bufs.dk, bufs.dv):
+            assert float(t[:, s:e].abs().max()) == 0.0
+
+
 def test_bf16_qwen3_4b_layer_two_groups():
     w = workloads.WORKLOADS["qwen3-4b-layer-t8192-c512"]
     cpu = inputs.layer_inputs(w)
