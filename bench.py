@@ -33,7 +33,7 @@ FALLBACK_SUSTAINED_TFLOPS = 1700.0   # used only when no measured peaks file exi
 # DRAM traffic (bytes read + written) per backward launch, from the ncu
 # launch list of the bench workload (average over its 16 chunk launches);
 # set to None whenever the kernel changes until it is measured again.
-BWD_TRAFFIC_BYTES_PER_LAUNCH = None   # bwd_bf16_kernel grid order changed: not yet measured
+BWD_TRAFFIC_BYTES_PER_LAUNCH = 466.3e6   # bwd_bf16_kernel<128>, prefix tiles first per head, diagonal tiles last
 
 
 def parse_args():
@@ -212,15 +212,23 @@ def run_ours(args, w):
     D = len(starts)
     T, c = w.seq, w.chunk
 
+    main = torch.cuda.current_stream()
+    side = binding.side_streams(dev, 1)[0]
+
     def step(events=None):
         binding.reset_accum(bufs.dk, bufs.dv, w.hq)
+        # chunk forwards alternate over two streams (binding.forward_chunks);
+        # the forward is timed as a phase, from the fork to the join
+        if events is not None:
+            events["fwd"][0].record(main)
+        side.wait_stream(main)
         for i, s in enumerate(starts):
             e = min(s + c, T)
-            if events is not None:
-                events["fwd"][i][0].record()
-            binding.chunk_fwd(q[:, s:e], k, v, bufs.o[:, s:e], bufs.lse_chunks[i], s)
-            if events is not None:
-                events["fwd"][i][1].record()
+            binding.chunk_fwd(q[:, s:e], k, v, bufs.o[:, s:e], bufs.lse_chunks[i], s,
+                              stream=main if i % 2 == 0 else side)
+        main.wait_stream(side)
+        if events is not None:
+            events["fwd"][1].record(main)
         for i in range(D - 1, -1, -1):
             s = starts[i]
             e = min(s + c, T)
@@ -241,8 +249,7 @@ def run_ours(args, w):
     def ev():
         return torch.cuda.Event(enable_timing=True)
 
-    launch_ev = [{"fwd": [(ev(), ev()) for _ in range(D)], "bwd": [(ev(), ev()) for _ in range(D)]}
-                 for _ in range(args.steps)]
+    launch_ev = [{"fwd": (ev(), ev()), "bwd": [(ev(), ev()) for _ in range(D)]} for _ in range(args.steps)]
     gpu_id = None
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -268,7 +275,7 @@ def run_ours(args, w):
     value = world * flops_rank * args.steps / (ms / 1e3) / 1e12
 
     # per-launch roofline (live CUDA-event durations inside the timed region)
-    fwd_ms = sum(a.elapsed_time(b) for e in launch_ev for a, b in e["fwd"])
+    fwd_ms = sum(e["fwd"][0].elapsed_time(e["fwd"][1]) for e in launch_ev)
     bwd_ms = sum(a.elapsed_time(b) for e in launch_ev for a, b in e["bwd"])
     pairs = sum(workloads.causal_pairs(s, min(c, T - s)) for s in starts)
     fwd_flops = 4 * w.batch * w.hq * w.head_dim * pairs * args.steps
@@ -284,7 +291,9 @@ def run_ours(args, w):
                 "avg_launch_ms": bwd_ms / (D * args.steps)}
     roofline_fwd = {"kernel": "seqattn_chunk_fwd (fwd_bf16_kernel)", "bound": "tensor", "achieved": fwd_tf,
                     "peak": peak, "unit": "TFLOP/s", "frac": fwd_tf / peak,
-                    "avg_launch_ms": fwd_ms / (D * args.steps)}
+                    "per_phase": f"causal fwd FLOPs 4*Hq*d*pairs over the {D} chunk forwards of a step, "
+                                 "timed from the two-stream fork to the join",
+                    "phase_ms": fwd_ms / args.steps}
 
     # end to end through the public API with pinned host buffers: inputs are
     # uploaded chunk by chunk ahead of the forward calls and every output

@@ -233,24 +233,55 @@ def _rows(t, s, e):
     return v if v.is_contiguous() else v.contiguous()
 
 
+_side_streams = {}
+
+
+def side_streams(device, n):
+    """``n`` long-lived side streams of ``device`` (created once)."""
+    key = torch.device(device).index if torch.device(device).index is not None else torch.cuda.current_device()
+    have = _side_streams.setdefault(key, [])
+    while len(have) < n:
+        have.append(torch.cuda.Stream(device=key))
+    return have[:n]
+
+
+def forward_chunks(q, k, v, chunk, bufs, scale=None, stream=None, fwd_streams=2):
+    """Forward every chunk into ``bufs``.  The chunk forwards depend only on
+    the caches (StreamBP review page, Property 3.1), so chunk i runs on stream
+    i % fwd_streams (``stream`` and side streams forked from it): the last,
+    partly filled wave of one chunk's grid overlaps the next chunk's.  All
+    streams are joined back into ``stream`` before returning."""
+    B, T, Hq, d = q.shape
+    main = stream if stream is not None else torch.cuda.current_stream()
+    sides = side_streams(q.device, fwd_streams - 1)
+    for sd in sides:
+        sd.wait_stream(main)
+    for i, s in enumerate(bufs.starts):
+        e = min(s + chunk, T)
+        st = main if i % fwd_streams == 0 else sides[i % fwd_streams - 1]
+        o_c = bufs.o[:, s:e]
+        if o_c.is_contiguous():
+            chunk_fwd(_rows(q, s, e), k, v, o_c, bufs.lse_chunks[i], s, s, scale, st)
+        else:
+            with torch.cuda.stream(st):
+                tmp = torch.empty_like(o_c.contiguous())
+                chunk_fwd(_rows(q, s, e), k, v, tmp, bufs.lse_chunks[i], s, s, scale, st)
+                o_c.copy_(tmp)
+    for sd in sides:
+        main.wait_stream(sd)
+
+
 def layer_forward_backward(q, k, v, d_o, chunk, scale=None, bufs=None, stream=None,
-                           bwd_order="descending"):
+                           bwd_order="descending", fwd_streams=2):
     """One pass of the chunked layer: reset the running sums, forward chunks
-    0..D-1, backward chunks D-1..0 (SeCO's last-to-first relay order).
-    Returns the LayerBuffers holding O, per-chunk LSE, dQ, dK, dV."""
+    0..D-1 (over ``fwd_streams`` streams), backward chunks D-1..0 (SeCO's
+    last-to-first relay order).  Returns the LayerBuffers holding O,
+    per-chunk LSE, dQ, dK, dV."""
     B, T, Hq, d = q.shape
     if bufs is None:
         bufs = LayerBuffers(q, k, chunk)
     reset_accum(bufs.dk, bufs.dv, Hq, stream)
-    for i, s in enumerate(bufs.starts):
-        e = min(s + chunk, T)
-        o_c = bufs.o[:, s:e]
-        if o_c.is_contiguous():
-            chunk_fwd(_rows(q, s, e), k, v, o_c, bufs.lse_chunks[i], s, s, scale, stream)
-        else:
-            tmp = torch.empty_like(o_c.contiguous())
-            chunk_fwd(_rows(q, s, e), k, v, tmp, bufs.lse_chunks[i], s, s, scale, stream)
-            o_c.copy_(tmp)
+    forward_chunks(q, k, v, chunk, bufs, scale, stream, fwd_streams)
     order = list(enumerate(bufs.starts))
     if bwd_order == "descending":
         order = order[::-1]
@@ -291,15 +322,7 @@ def spaco_layer_forward_backward(q, k, v, d_o, chunk, selected, factor=None, sca
     if factor is None:
         factor = spaco_factor(n_chunks, len(chosen))
     reset_accum(bufs.dk, bufs.dv, Hq, stream)
-    for i, s in enumerate(bufs.starts):
-        e = min(s + chunk, T)
-        o_c = bufs.o[:, s:e]
-        if o_c.is_contiguous():
-            chunk_fwd(_rows(q, s, e), k, v, o_c, bufs.lse_chunks[i], s, s, scale, stream)
-        else:
-            tmp = torch.empty_like(o_c.contiguous())
-            chunk_fwd(_rows(q, s, e), k, v, tmp, bufs.lse_chunks[i], s, s, scale, stream)
-            o_c.copy_(tmp)
+    forward_chunks(q, k, v, chunk, bufs, scale, stream)
     for i, s in reversed(list(enumerate(bufs.starts))):
         e = min(s + chunk, T)
         dq_c = bufs.dq[:, s:e]
@@ -409,16 +432,21 @@ class HostLayerPass:
                 ev.record(self.up)
                 ev_do.append(ev)
         reset_accum(b.dk, b.dv, q.shape[2], main)
+        # chunk forwards alternate over two compute streams (see forward_chunks)
+        side = side_streams(q.device, 1)[0]
+        side.wait_stream(main)
         for i, s in enumerate(starts):
             e = min(s + c, T)
-            main.wait_event(ev_in[i])
-            chunk_fwd(_rows(q, s, e), k, v, b.o[:, s:e], b.lse_chunks[i], s, s, None, main)
+            st = main if i % 2 == 0 else side
+            st.wait_event(ev_in[i])
+            chunk_fwd(_rows(q, s, e), k, v, b.o[:, s:e], b.lse_chunks[i], s, s, None, st)
             ev = torch.cuda.Event()
-            ev.record(main)
+            ev.record(st)
             self.down.wait_event(ev)
             with torch.cuda.stream(self.down):
                 self.h_o[:, s:e].copy_(b.o[:, s:e], non_blocking=True)
                 self.h_lse[i].copy_(b.lse_chunks[i], non_blocking=True)
+        main.wait_stream(side)
         for i in range(len(starts) - 1, -1, -1):
             s = starts[i]
             e = min(s + c, T)

@@ -95,6 +95,7 @@ struct BwdParams {
   int q_start, kv_begin;
   int n_ktiles;
   int n_q64;               // 64-row query tiles of the chunk (the last may be partial)
+  int n_pre;               // key tiles wholly before the chunk's first row
   float scale;
   float scale_log2;
   const float* stats;      // [B, Hq, n_q64, 2, 64]: -L log2 e, then Delta, per query tile
@@ -175,14 +176,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int abort_flag;
   Watchdog wd{&abort_flag, p.err};
 
-  // ---- work item: kv head g (fastest), key tile kt, batch b.  Key tiles of
-  // the prefix (the longest loops) start first and the shorter diagonal
-  // tiles fill the last wave.
-  int idx = blockIdx.x;
-  const int g = idx % p.Hkv;
-  idx /= p.Hkv;
-  const int kt = idx % p.n_ktiles;
-  const int b = idx / p.n_ktiles;
+  // ---- work item: (batch b, kv head g, key tile kt).
+  // Per batch entry: first the key tiles that lie wholly before the chunk
+  // (all of equal, longest length), key tile fastest within each key/value
+  // head so that a wave shares one group's Q, dO and dq in L2; then the tiles
+  // that reach into the chunk (shorter, decreasing), head fastest, so the
+  // shortest loops form the last wave.
+  const int per_b = p.n_ktiles * p.Hkv;
+  const int b = blockIdx.x / per_b;
+  const int idx = blockIdx.x - b * per_b;
+  int g, kt;
+  if (idx < p.n_pre * p.Hkv) {
+    g = idx / p.n_pre;
+    kt = idx - g * p.n_pre;
+  } else {
+    const int j = idx - p.n_pre * p.Hkv;
+    kt = p.n_pre + j / p.Hkv;
+    g = j - (j / p.Hkv) * p.Hkv;
+  }
   const int kb = p.kv_begin + kt * kBK;                  // absolute first key of the tile
   const int q_end = p.q_start + p.q_len;                 // one past the chunk's last row
   // first query tile that sees any key of this tile (the one holding row kb)
@@ -548,6 +559,7 @@ cudaError_t launch_bwd_bf16(const ChunkGeom& g, const Bf16BwdMaps& maps, const f
   p.kv_begin = static_cast<int>(g.kv_begin);
   p.n_ktiles = static_cast<int>((g.q_start + g.q_len - g.kv_begin + kBK - 1) / kBK);
   p.n_q64 = static_cast<int>((g.q_len + kBQ - 1) / kBQ);
+  p.n_pre = static_cast<int>((g.q_start - g.kv_begin) / kBK);   // tiles with kb + 127 < q_start
   p.scale = g.scale;
   p.scale_log2 = g.scale * 1.4426950408889634f;
   p.stats = stats;
