@@ -4,7 +4,8 @@ This module holds no attention arithmetic: it only draws random tensors.  It
 is the one module that both the CUDA-path tests/benchmark and the CPU oracle
 checks take their inputs from.
 
-Recipe: Q, K, V and dO are iid N(0, 1).  Each tensor is drawn in blocks of
+Recipe: Q, K, V and dO (and the hidden states H that feed the projections,
+drawn as one head of d_model columns) are iid N(0, 1).  Each tensor is drawn in blocks of
 ``BLOCK_ROWS`` sequence rows per batch entry; every block has its own
 ``torch.Generator`` seeded with a 32-bit SplitMix64 hash of (seed, tensor id,
 batch entry, block index),
@@ -16,7 +17,7 @@ float32 and then cast to the workload dtype with round-to-nearest-even.
 import torch
 
 BLOCK_ROWS = 1024
-TENSOR_IDS = {"q": 0, "k": 1, "v": 2, "do": 3}
+TENSOR_IDS = {"q": 0, "k": 1, "v": 2, "do": 3, "h": 4}
 
 _DTYPES = {"bf16": torch.bfloat16, "fp32": torch.float32}
 

@@ -53,6 +53,7 @@ __all__ = [
     "chunk_backward",
     "chunked_layer",
     "sparse_chunked_layer",
+    "projection_wgrad",
     "dense_causal_attention",
     "dense_causal_attention_grad",
     "row_forward",
@@ -215,6 +216,26 @@ def sparse_chunked_layer(q, k, v, do, chunk, scale, selected, factor):
             dk[:, s:e] = 0.0
             dv[:, s:e] = 0.0
     return o, lse, dq, dk, dv
+
+
+def projection_wgrad(h, g):
+    """Weight gradient of a projection X = H W from the gradient G of its
+    output: dW = sum over batch entries and rows of H[b, r]^T G[b, r].
+
+    This is the step after the path (SeCO review page, major comment 1 on
+    Algorithm 2: once chunk i's cache gradient is complete, chunk i's graph --
+    here its Q/K/V projections -- is backpropagated).  With G = dQ it gives
+    dW_q; with the finished dK / dV rows it gives dW_k / dW_v.  The sum over
+    rows splits over chunks, so chunk-by-chunk accumulation gives the same.
+
+    h: [B, T, d_model]; g: [B, T, n] (any trailing head dims flattened).
+    Returns dW [d_model, n] in float64."""
+    h = _as64(h)
+    g = _as64(g)
+    B, T = h.shape[:2]
+    h2 = h.reshape(B * T, -1)
+    g2 = g.reshape(B * T, -1)
+    return h2.T @ g2
 
 
 def dense_causal_attention(q, k, v, scale):

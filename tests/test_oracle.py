@@ -349,6 +349,54 @@ def test_spaco_pin_catches_a_compensated_direct_term():
     assert np.abs(bad - dk).max() > 1e-3 and np.abs(edk - dk).max() < 1e-12
 
 
+# ---------------------------------------------------------------- projection weight gradients
+
+def test_projection_wgrad_matches_autograd_through_the_projections():
+    """A tiny float64 model: Q = H W_q, K = H W_k, V = H W_v feed causal GQA
+    attention and L = sum dO o O.  torch autograd's dW_q, dW_k, dW_v equal
+    H^T dQ, H^T dK, H^T dV with dQ, dK, dV from the chunked oracle."""
+    B, T, dm, Hq, Hkv, d = 2, 10, 6, 4, 2, 3
+    rng = np.random.default_rng(51)
+    h = rng.standard_normal((B, T, dm))
+    wq, wk, wv = (rng.standard_normal((dm, n)) for n in (Hq * d, Hkv * d, Hkv * d))
+    do = rng.standard_normal((B, T, Hq, d))
+    scale = d ** -0.5
+    th = torch.tensor(h)
+    tw = [torch.tensor(w, requires_grad=True) for w in (wq, wk, wv)]
+    q = (th @ tw[0]).view(B, T, Hq, d)
+    k = (th @ tw[1]).view(B, T, Hkv, d)
+    v = (th @ tw[2]).view(B, T, Hkv, d)
+    kk = k.repeat_interleave(Hq // Hkv, dim=2)
+    vv = v.repeat_interleave(Hq // Hkv, dim=2)
+    s = torch.einsum("bihe,bjhe->bhij", q, kk) * scale
+    mask = torch.ones(T, T, dtype=torch.bool).tril()
+    p = torch.softmax(s.masked_fill(~mask, float("-inf")), dim=-1)
+    o = torch.einsum("bhij,bjhe->bihe", p, vv)
+    (o * torch.tensor(do)).sum().backward()
+    _, _, dq, dk, dv = oracle.chunked_layer(q.detach().numpy(), k.detach().numpy(), v.detach().numpy(), do, 4,
+                                            scale)
+    for w, g in zip(tw, (dq, dk, dv)):
+        np.testing.assert_allclose(oracle.projection_wgrad(h, g), w.grad.numpy(), rtol=0, atol=1e-11)
+
+
+def test_projection_wgrad_splits_over_chunks_and_matches_loops():
+    """The row sum splits over chunks (the relay order runs it chunk by chunk),
+    and equals the element-wise triple loop on a tiny case."""
+    rng = np.random.default_rng(53)
+    h = rng.standard_normal((2, 7, 3))
+    g = rng.standard_normal((2, 7, 4))
+    full = oracle.projection_wgrad(h, g)
+    parts = sum(oracle.projection_wgrad(h[:, s:s + 3], g[:, s:s + 3]) for s in range(0, 7, 3))
+    np.testing.assert_allclose(parts, full, rtol=0, atol=1e-12)
+    loops = np.zeros((3, 4))
+    for b in range(2):
+        for r in range(7):
+            for i in range(3):
+                for j in range(4):
+                    loops[i, j] += h[b, r, i] * g[b, r, j]
+    np.testing.assert_allclose(full, loops, rtol=0, atol=1e-12)
+
+
 # ---------------------------------------------------------------- input generator
 
 def test_inputs_are_seeded_and_block_addressable():
