@@ -45,6 +45,7 @@ def parse_args():
     ap.add_argument("--workload", default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-wgrad", action="store_true")
     return ap.parse_args()
 
 
@@ -323,6 +324,43 @@ def run_ours(args, w):
                "api": "binding.HostLayerPass (pinned host in/out, copies overlapped with compute)"}
         del hp
 
+    # the step after the path: the projections' weight gradients in the relay
+    # (dW_q, dW_k, dW_v += H^(i)T dQ^(i), dK^(i), dV^(i) after chunk i's
+    # backward), timed alone over one pass worth of chunks, with synthetic
+    # hidden states H of d_model = Hq d columns; outside the headline metric
+    wgrad = None
+    if not args.no_wgrad:
+        dm = w.hq * w.head_dim
+        h = inputs.draw("h", seed, w.batch, w.seq, 1, dm, torch.bfloat16, dev)[:, :, 0].contiguous()
+        dws = [torch.zeros((dm, n), device=dev) for n in (w.hq * w.head_dim, w.hkv * w.head_dim,
+                                                         w.hkv * w.head_dim)]
+        ws = torch.empty(binding.wgrad_workspace_size(w.batch, c, dm), dtype=torch.uint8, device=dev)
+
+        def wgrad_pass():
+            for i in range(D - 1, -1, -1):
+                s = starts[i]
+                e = min(s + c, T)
+                for g, dw in ((bufs.dq, dws[0]), (bufs.dk, dws[1]), (bufs.dv, dws[2])):
+                    binding.proj_wgrad(h, g, dw, s, e, ws)
+
+        for _ in range(2):
+            wgrad_pass()
+        torch.cuda.synchronize()
+        a, b = ev(), ev()
+        a.record()
+        for _ in range(args.steps):
+            wgrad_pass()
+        b.record()
+        torch.cuda.synchronize()
+        binding.sync_status()
+        wg_ms = a.elapsed_time(b) / args.steps
+        wg_flops = 2.0 * w.batch * w.seq * dm * (w.hq + 2 * w.hkv) * w.head_dim
+        wgrad = {"metric": "projection weight-gradient TFLOP/s (dW_q, dW_k, dW_v of one pass)",
+                 "value": wg_flops / (wg_ms / 1e3) / 1e12, "unit": UNIT, "ms_per_pass": wg_ms,
+                 "d_model": dm, "kernels": "rows_to_bf16_kernel + cuBLASLt bf16 GEMM (float32 accumulate)",
+                 "launches_per_pass": 6 * D}
+        del h, dws, ws
+
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         G = w.hq // w.hkv
@@ -338,7 +376,7 @@ def run_ours(args, w):
         "config": workload_config(w),
         "frac_of_peak": value / world / peak,
         "roofline": roofline, "roofline_fwd": roofline_fwd,
-        "cpu_baseline": cpu_baseline, "e2e": e2e,
+        "cpu_baseline": cpu_baseline, "e2e": e2e, "wgrad": wgrad,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clock_info,
     }

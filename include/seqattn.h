@@ -166,6 +166,34 @@ seqattn_status seqattn_scale_accum_rows(const seqattn_problem* pb, int64_t row_b
                                         int64_t row_end, float scale, float* dk_accum,
                                         float* dv_accum, seqattn_stream_t stream);
 
+/*
+ * Projection weight gradient of rows [row_begin, row_end): the step after the
+ * path (SeCO review page, major comment 1 on Algorithm 2 -- once chunk i's
+ * cache gradient is complete, chunk i's graph, here the Q/K/V projections
+ * X = H W, is backpropagated).  With the last-to-first chunk order the dK/dV
+ * rows of chunk i are final right after its backward, so this runs per chunk.
+ *   dw[d_model, n] += sum over batch entries b and rows r of h[b, r]^T g[b, r]
+ *   h: [batch, seq_len, d_model] bf16 (the projections' input)
+ *   g: [batch, seq_len, n] float32 (dQ with n = Hq d, or dK / dV with
+ *      n = Hkv d)
+ *   dw: [d_model, n] float32, row-major, accumulated (never overwritten)
+ * g is rounded to bf16 (nearest even) into the workspace, then a cuBLASLt
+ * bf16 GEMM with float32 accumulation adds into dw, one GEMM per batch entry.
+ * Requires batch >= 1, 0 <= row_begin <= row_end <= seq_len, d_model and n
+ * positive multiples of 8, 16-byte aligned pointers, and a 256-byte aligned
+ * workspace of at least seqattn_proj_wgrad_workspace_size(batch,
+ * row_end - row_begin, n) bytes.  Async on `stream`; INVALID_ARG before any
+ * launch on a bad argument, SEQATTN_ERR_CUDA if cuBLASLt fails.
+ */
+seqattn_status seqattn_proj_wgrad(int32_t batch, int64_t seq_len, int64_t row_begin,
+                                  int64_t row_end, int32_t d_model, int32_t n, const void* h,
+                                  const float* g, float* dw, void* workspace,
+                                  size_t workspace_bytes, seqattn_stream_t stream);
+
+/* Bytes of workspace seqattn_proj_wgrad needs (0 for invalid sizes).  Pure
+ * host function. */
+size_t seqattn_proj_wgrad_workspace_size(int32_t batch, int64_t rows, int32_t n);
+
 /* Bytes of workspace seqattn_chunk_bwd needs for a chunk of q_len rows
  * (0 for an invalid problem).  Pure host function. */
 size_t seqattn_bwd_workspace_size(const seqattn_problem* pb, int64_t q_len);

@@ -28,6 +28,8 @@ EXPORTED = (
     "seqattn_chunk_bwd_noalloc",
     "seqattn_reset_accum",
     "seqattn_scale_accum_rows",
+    "seqattn_proj_wgrad",
+    "seqattn_proj_wgrad_workspace_size",
     "seqattn_bwd_workspace_size",
     "seqattn_sync_status",
     "seqattn_status_string",
@@ -78,6 +80,11 @@ def load_library(path=LIB_PATH):
     lib.seqattn_reset_accum.restype = ctypes.c_int
     lib.seqattn_scale_accum_rows.argtypes = [P, i64, i64, f32, vp, vp, vp]
     lib.seqattn_scale_accum_rows.restype = ctypes.c_int
+    i32 = ctypes.c_int32
+    lib.seqattn_proj_wgrad.argtypes = [i32, i64, i64, i64, i32, i32, vp, vp, vp, vp, sz, vp]
+    lib.seqattn_proj_wgrad.restype = ctypes.c_int
+    lib.seqattn_proj_wgrad_workspace_size.argtypes = [i32, i64, i32]
+    lib.seqattn_proj_wgrad_workspace_size.restype = sz
     lib.seqattn_bwd_workspace_size.argtypes = [P, i64]
     lib.seqattn_bwd_workspace_size.restype = sz
     lib.seqattn_sync_status.argtypes = [vp]
@@ -196,6 +203,29 @@ def scale_accum_rows(dk_accum, dv_accum, row_begin, row_end, scale, stream=None)
                                                    _ptr(dk_accum), _ptr(dv_accum), _stream(stream)))
 
 
+def wgrad_workspace_size(batch, rows, n):
+    """Bytes of workspace ``proj_wgrad`` needs for ``rows`` rows of width ``n``."""
+    return int(load_library().seqattn_proj_wgrad_workspace_size(batch, rows, n))
+
+
+def proj_wgrad(h, g, dw, row_begin, row_end, workspace=None, stream=None):
+    """dw [d_model, n] += sum over batch entries of h[b, r0:r1]^T g[b, r0:r1],
+    with h [B, T, d_model] bf16 (hidden states) and g [B, T, ...] float32 (dQ,
+    dK or dV; trailing dims flattened to n)."""
+    B, T, dm = h.shape
+    n = g[0, 0].numel()
+    _need(h, "h", torch.bfloat16)
+    _need(g, "g", torch.float32)
+    _need(dw, "dw", torch.float32, (dm, n))
+    if tuple(g.shape[:2]) != (B, T):
+        raise ValueError(f"g has leading shape {tuple(g.shape[:2])}, expected {(B, T)}")
+    need = wgrad_workspace_size(B, row_end - row_begin, n)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=h.device)
+    _check(load_library().seqattn_proj_wgrad(B, T, row_begin, row_end, dm, n, _ptr(h), _ptr(g), _ptr(dw),
+                                             _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
 def sync_status(stream=None):
     """Synchronise the stream and raise if a kernel gave up a bounded wait."""
     _check(load_library().seqattn_sync_status(_stream(stream)))
@@ -272,19 +302,31 @@ def forward_chunks(q, k, v, chunk, bufs, scale=None, stream=None, fwd_streams=2)
 
 
 def layer_forward_backward(q, k, v, d_o, chunk, scale=None, bufs=None, stream=None,
-                           bwd_order="descending", fwd_streams=2):
+                           bwd_order="descending", fwd_streams=2, wgrad=None):
     """One pass of the chunked layer: reset the running sums, forward chunks
     0..D-1 (over ``fwd_streams`` streams), backward chunks D-1..0 (SeCO's
     last-to-first relay order).  Returns the LayerBuffers holding O,
-    per-chunk LSE, dQ, dK, dV."""
+    per-chunk LSE, dQ, dK, dV.
+
+    ``wgrad = (h, dw_q, dw_k, dw_v)`` also runs the projections' weight
+    gradients in the relay: right after chunk i's backward, its dQ rows and
+    its dK/dV rows are final (every later chunk has run), so
+    dw_x += H^(i)T dX^(i) is added for each of the three (h: [B, T, d_model]
+    bf16; dw_q: [d_model, Hq d], dw_k, dw_v: [d_model, Hkv d], float32,
+    accumulated).  Needs the descending order."""
     B, T, Hq, d = q.shape
     if bufs is None:
         bufs = LayerBuffers(q, k, chunk)
+    if wgrad is not None and bwd_order != "descending":
+        raise ValueError("the projection gradients run in the last-to-first relay order")
     reset_accum(bufs.dk, bufs.dv, Hq, stream)
     forward_chunks(q, k, v, chunk, bufs, scale, stream, fwd_streams)
     order = list(enumerate(bufs.starts))
     if bwd_order == "descending":
         order = order[::-1]
+    ws = None
+    if wgrad is not None:
+        ws = torch.empty(wgrad_workspace_size(B, chunk, Hq * d), dtype=torch.uint8, device=q.device)
     for i, s in order:
         e = min(s + chunk, T)
         dq_c = bufs.dq[:, s:e]
@@ -293,6 +335,10 @@ def layer_forward_backward(q, k, v, d_o, chunk, scale=None, bufs=None, stream=No
                   tgt, bufs.dk, bufs.dv, s, s, scale, bufs.workspace, stream)
         if tgt is not dq_c:
             dq_c.copy_(tgt)
+        if wgrad is not None:
+            h, dw_q, dw_k, dw_v = wgrad
+            for g, dw in ((bufs.dq, dw_q), (bufs.dk, dw_k), (bufs.dv, dw_v)):
+                proj_wgrad(h, g, dw, s, e, ws, stream)
     return bufs
 
 

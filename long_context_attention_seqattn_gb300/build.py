@@ -17,7 +17,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libseqattn.so")
 
-SOURCES = ["seqattn_api.cu", "simt_f32.cu", "fwd_bf16.cu", "bwd_bf16.cu"]
+SOURCES = ["seqattn_api.cu", "simt_f32.cu", "fwd_bf16.cu", "bwd_bf16.cu", "wgrad.cu"]
+LIBS = ["-lcublasLt"]
 HEADERS = ["internal.h", "sm103_ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -39,7 +40,7 @@ def _fingerprint():
             h.update(f.encode() + fh.read())
     with open(os.path.join(INCLUDE, "seqattn.h"), "rb") as fh:
         h.update(fh.read())
-    h.update(" ".join(ARCH + CFLAGS).encode())
+    h.update(" ".join(ARCH + CFLAGS + LIBS).encode())
     return h.hexdigest()
 
 
@@ -71,7 +72,7 @@ def build(force=False, verbose=False):
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
     tmp = LIB_PATH + ".tmp"
-    cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + [o for _, o, _ in results]
+    cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + [o for _, o, _ in results] + LIBS
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -54,4 +54,17 @@ cudaError_t launch_fwd_bf16(const ChunkGeom& g, const Bf16FwdMaps& maps, void* o
 cudaError_t launch_bwd_bf16(const ChunkGeom& g, const Bf16BwdMaps& maps, const float* stats,
                             float* dq, float* dk, float* dv, unsigned int* err, cudaStream_t s);
 
+// ---- projection weight gradient (cuBLASLt bf16 GEMM) ----------------------
+// cuBLASLt's own scratch, carved from the caller's workspace after the bf16
+// copy of G.
+constexpr size_t kWgradLtWorkspace = size_t(32) << 20;
+struct WgradStatus {
+  cudaError_t cuda = cudaSuccess;
+  int blas = 0;  // cublasStatus_t
+};
+size_t wgrad_workspace_bytes(int32_t batch, int64_t rows, int32_t n);
+WgradStatus launch_wgrad(int32_t batch, int64_t seq_len, int64_t row_begin, int64_t row_end, int32_t d_model,
+                         int32_t n, const void* h, const float* g, float* dw, void* workspace,
+                         size_t workspace_bytes, cudaStream_t s);
+
 }  // namespace seqattn

@@ -264,6 +264,37 @@ seqattn_status seqattn_scale_accum_rows(const seqattn_problem* pb, int64_t row_b
   return e == cudaSuccess ? ok() : cuda_fail(e, "scale launch");
 }
 
+size_t seqattn_proj_wgrad_workspace_size(int32_t batch, int64_t rows, int32_t n) {
+  if (batch < 1 || rows < 0 || n < 8 || n % 8) return 0;
+  return wgrad_workspace_bytes(batch, rows, n);
+}
+
+seqattn_status seqattn_proj_wgrad(int32_t batch, int64_t seq_len, int64_t row_begin,
+                                  int64_t row_end, int32_t d_model, int32_t n, const void* h,
+                                  const float* g, float* dw, void* workspace,
+                                  size_t workspace_bytes, seqattn_stream_t stream) {
+  if (batch < 1 || seq_len < 1) return fail(SEQATTN_ERR_INVALID_ARG, "batch and seq_len must be >= 1");
+  if (row_begin < 0 || row_end < row_begin || row_end > seq_len)
+    return fail(SEQATTN_ERR_INVALID_ARG, "need 0 <= row_begin <= row_end <= seq_len (got %lld, %lld)",
+                (long long)row_begin, (long long)row_end);
+  if (d_model < 8 || d_model % 8 || n < 8 || n % 8)
+    return fail(SEQATTN_ERR_INVALID_ARG, "d_model (%d) and n (%d) must be positive multiples of 8", d_model, n);
+  if (static_cast<int64_t>(batch) * seq_len > INT32_MAX)
+    return fail(SEQATTN_ERR_INVALID_ARG, "batch * seq_len exceeds 2^31 - 1 rows");
+  seqattn_status s = check_ptrs({{h, "h"}, {g, "g"}, {dw, "dw"}, {workspace, "workspace"}});
+  if (s != SEQATTN_OK) return s;
+  const int64_t rows = row_end - row_begin;
+  if (workspace_bytes < wgrad_workspace_bytes(batch, rows, n))
+    return fail(SEQATTN_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes,
+                wgrad_workspace_bytes(batch, rows, n));
+  if (rows == 0) return ok();
+  WgradStatus w = launch_wgrad(batch, seq_len, row_begin, row_end, d_model, n, h, g, dw, workspace, workspace_bytes,
+                               reinterpret_cast<cudaStream_t>(stream));
+  if (w.cuda != cudaSuccess) return cuda_fail(w.cuda, "wgrad conversion launch");
+  if (w.blas != 0) return fail(SEQATTN_ERR_CUDA, "cuBLASLt returned status %d", w.blas);
+  return ok();
+}
+
 size_t seqattn_bwd_workspace_size(const seqattn_problem* pb, int64_t q_len) {
   if (check_problem(pb) != SEQATTN_OK || q_len < 0) return 0;
   return workspace_bytes(pb, q_len);

@@ -293,6 +293,50 @@ def test_spaco_pass_matches_oracle(dtype, B, T, Hq, Hkv, d, chunk, selected, fac
             assert float(t[:, s:e].abs().max()) == 0.0
 
 
+def assert_wgrad(name, got, ref):
+    """Bars for a weight gradient: every element is a sum over many rows, so the
+    element-wise 5e-2 of the attention outputs does not apply; rel-L2 <= 2e-2
+    and max-abs <= 1e-2 of the largest |ref| (G is rounded to bf16, relative
+    error 2^-9 per term)."""
+    r, a = rel_l2(got, ref), max_abs(got, ref)
+    assert r <= BF16_REL and a <= 1e-2 * float(np.abs(ref).max()), f"{name}: rel-L2 {r:.3e} max-abs {a:.3e}"
+
+
+def test_proj_wgrad_accumulates_h_transpose_g():
+    """dw += h^T g over a row range of every batch entry, twice (accumulation),
+    against the float64 oracle."""
+    B, T, dm, n, r0, r1 = 2, 300, 96, 136, 37, 261
+    h = inputs.draw("h", 5, B, T, 1, dm, torch.bfloat16)[:, :, 0]
+    g = inputs.draw("do", 5, B, T, 1, n, torch.float32)[:, :, 0]
+    dw = torch.zeros((dm, n), device="cuda")
+    hd, gd = h.cuda().contiguous(), g.cuda().contiguous()
+    binding.proj_wgrad(hd, gd, dw, r0, r1)
+    binding.proj_wgrad(hd, gd, dw, r0, r1)
+    binding.sync_status()
+    ref = 2 * oracle.projection_wgrad(h[:, r0:r1].double().numpy(), g[:, r0:r1].double().numpy())
+    assert_wgrad("dW", cpu64(dw), ref)
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,d,dm,chunk", [
+    (1, 512, 4, 2, 128, 256, 128),
+    (2, 300, 4, 1, 64, 64, 100),       # ragged last chunk, d = 64, batch 2
+])
+def test_layer_pass_with_projection_wgrad(B, T, Hq, Hkv, d, dm, chunk):
+    """The relay pass with the projections' weight gradients: after chunk i's
+    backward, dW_q, dW_k, dW_v += H^(i)T (dQ, dK, dV rows of chunk i).  The
+    sum over chunks equals the oracle's H^T dQ, H^T dK, H^T dV."""
+    cpu = small_inputs(B, T, Hq, Hkv, d, "bf16", 88)
+    h = inputs.draw("h", 88, B, T, 1, dm, torch.bfloat16)[:, :, 0]
+    dws = [torch.zeros((dm, n), device="cuda") for n in (Hq * d, Hkv * d, Hkv * d)]
+    bufs = binding.layer_forward_backward(*[x.cuda() for x in cpu], chunk,
+                                          wgrad=(h.cuda().contiguous(), *dws))
+    binding.sync_status()
+    _, _, dq, dk, dv = oracle.chunked_layer(*(x.to(torch.float64).numpy() for x in cpu), chunk, d ** -0.5)
+    hn = h.double().numpy()
+    for name, got, g in zip(("dW_q", "dW_k", "dW_v"), dws, (dq, dk, dv)):
+        assert_wgrad(name, cpu64(got), oracle.projection_wgrad(hn, g))
+
+
 def test_bf16_qwen3_4b_layer_two_groups():
     w = workloads.WORKLOADS["qwen3-4b-layer-t8192-c512"]
     cpu = inputs.layer_inputs(w)
