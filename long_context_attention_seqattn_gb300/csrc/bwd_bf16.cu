@@ -372,12 +372,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c_off = half * 32;                        // first query column of this warp
     const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
     bool ok = true;
+    int st = 0, ph = 0;                                 // ring stage of step n and its phase parity
+    int qi = qi_first;                                  // query tile of step n (heads cycle slowest)
     for (int n = 0; n < n_steps; ++n) {
-      const int st = n % kQStages;
       const int bb = n & 1;
-      const int qi = step_qtile(n);
-      // -L log2(e) of the stage first: it loads while S^T computes
-      if (!(ok = warp_wait(wd, &bars.q_full[st], (n / kQStages) & 1))) break;
+      if (!(ok = warp_wait(wd, &bars.q_full[st], ph))) break;
+      if (!(ok = warp_wait(wd, &bars.s_full[bb], (n >> 1) & 1))) break;
+      tc_fence_after_sync();
+      const uint32_t cb = tmem + lane_base + col_buf(bb);
+      uint32_t r[32];
+      tmem_ld32(cb + kOffS + c_off, r);
+      // -L log2(e) of the step's rows, read while the TMEM load is in flight
       const float4* L4 = reinterpret_cast<const float4*>(stat + st * 2 * kBQ + c_off);
       const float4* D4 = reinterpret_cast<const float4*>(stat + st * 2 * kBQ + kBQ + c_off);
       uint64_t nl2[16];                                 // pairs of query rows
@@ -387,11 +392,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         nl2[2 * j] = f2_pack(l.x, l.y);
         nl2[2 * j + 1] = f2_pack(l.z, l.w);
       }
-      if (!(ok = warp_wait(wd, &bars.s_full[bb], (n >> 1) & 1))) break;
-      tc_fence_after_sync();
-      const uint32_t cb = tmem + lane_base + col_buf(bb);
-      uint32_t r[32];
-      tmem_ld32(cb + kOffS + c_off, r);
       const int q_abs0 = p.q_start + qi * kBQ + c_off;  // absolute row of this warp's column 0
       const bool masked = kb + kBK - 1 > q_abs0;        // some key of the tile follows some row
       tmem_ld_wait();
@@ -451,6 +451,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before_sync();
       mbar_arrive(&bars.ds_full[bb]);
+      if (++st == kQStages) {
+        st = 0;
+        ph ^= 1;
+      }
+      if (++qi == qi_first + nq) qi = qi_first;
     }
     // ---- epilogue: this tile's dK (half 0) or dV (half 1) rows into the running sums
     if (ok) ok = warp_wait(wd, &bars.acc_done, 0);
