@@ -214,20 +214,23 @@ def run_ours(args, w):
     T, c = w.seq, w.chunk
 
     main = torch.cuda.current_stream()
-    side = binding.side_streams(dev, 1)[0]
+    n_fwd = binding.auto_fwd_streams(q, c)
+    sides = binding.side_streams(dev, n_fwd - 1)
 
     def step(events=None):
         binding.reset_accum(bufs.dk, bufs.dv, w.hq)
-        # chunk forwards alternate over two streams (binding.forward_chunks);
-        # the forward is timed as a phase, from the fork to the join
+        # chunk forwards spread over streams as in binding.forward_chunks; the
+        # forward is timed as a phase, from the fork to the join
         if events is not None:
             events["fwd"][0].record(main)
-        side.wait_stream(main)
+        for sd in sides:
+            sd.wait_stream(main)
         for i, s in enumerate(starts):
             e = min(s + c, T)
-            binding.chunk_fwd(q[:, s:e], k, v, bufs.o[:, s:e], bufs.lse_chunks[i], s,
-                              stream=main if i % 2 == 0 else side)
-        main.wait_stream(side)
+            st = main if i % n_fwd == 0 else sides[i % n_fwd - 1]
+            binding.chunk_fwd(q[:, s:e], k, v, bufs.o[:, s:e], bufs.lse_chunks[i], s, stream=st)
+        for sd in sides:
+            main.wait_stream(sd)
         if events is not None:
             events["fwd"][1].record(main)
         for i in range(D - 1, -1, -1):
@@ -293,7 +296,7 @@ def run_ours(args, w):
     roofline_fwd = {"kernel": "seqattn_chunk_fwd (fwd_bf16_kernel)", "bound": "tensor", "achieved": fwd_tf,
                     "peak": peak, "unit": "TFLOP/s", "frac": fwd_tf / peak,
                     "per_phase": f"causal fwd FLOPs 4*Hq*d*pairs over the {D} chunk forwards of a step, "
-                                 "timed from the two-stream fork to the join",
+                                 f"timed from the {n_fwd}-stream fork to the join",
                     "phase_ms": fwd_ms / args.steps}
 
     # end to end through the public API with pinned host buffers: inputs are

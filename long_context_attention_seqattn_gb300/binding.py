@@ -275,13 +275,28 @@ def side_streams(device, n):
     return have[:n]
 
 
-def forward_chunks(q, k, v, chunk, bufs, scale=None, stream=None, fwd_streams=2):
+def auto_fwd_streams(q, chunk):
+    """Streams for the chunk forwards: at least two (one chunk's last wave
+    overlaps the next chunk's grid), and enough that the forward grids of the
+    chunks in flight together cover the SMs when a chunk's own grid is small
+    (128-row query tiles x heads x batch CTAs per chunk); at most eight."""
+    B, T, Hq, d = q.shape
+    ctas = max(1, -(-min(chunk, T) // 128)) * Hq * B
+    sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+    return max(2, min(8, -(-sms // ctas)))
+
+
+def forward_chunks(q, k, v, chunk, bufs, scale=None, stream=None, fwd_streams=None):
     """Forward every chunk into ``bufs``.  The chunk forwards depend only on
     the caches (StreamBP review page, Property 3.1), so chunk i runs on stream
     i % fwd_streams (``stream`` and side streams forked from it): the last,
-    partly filled wave of one chunk's grid overlaps the next chunk's.  All
-    streams are joined back into ``stream`` before returning."""
+    partly filled wave of one chunk's grid overlaps the next chunk's, and
+    small chunks run side by side.  ``fwd_streams`` defaults to
+    ``auto_fwd_streams``.  All streams are joined back into ``stream`` before
+    returning."""
     B, T, Hq, d = q.shape
+    if fwd_streams is None:
+        fwd_streams = auto_fwd_streams(q, chunk)
     main = stream if stream is not None else torch.cuda.current_stream()
     sides = side_streams(q.device, fwd_streams - 1)
     for sd in sides:
@@ -302,11 +317,11 @@ def forward_chunks(q, k, v, chunk, bufs, scale=None, stream=None, fwd_streams=2)
 
 
 def layer_forward_backward(q, k, v, d_o, chunk, scale=None, bufs=None, stream=None,
-                           bwd_order="descending", fwd_streams=2, wgrad=None):
+                           bwd_order="descending", fwd_streams=None, wgrad=None):
     """One pass of the chunked layer: reset the running sums, forward chunks
-    0..D-1 (over ``fwd_streams`` streams), backward chunks D-1..0 (SeCO's
-    last-to-first relay order).  Returns the LayerBuffers holding O,
-    per-chunk LSE, dQ, dK, dV.
+    0..D-1 (over ``fwd_streams`` streams, see ``forward_chunks``), backward
+    chunks D-1..0 (SeCO's last-to-first relay order).  Returns the
+    LayerBuffers holding O, per-chunk LSE, dQ, dK, dV.
 
     ``wgrad = (h, dw_q, dw_k, dw_v)`` also runs the projections' weight
     gradients in the relay: right after chunk i's backward, its dQ rows and
