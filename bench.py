@@ -287,7 +287,7 @@ def run_ours(args, w):
     peak, peak_src = measured_peak()
     bwd_tf = bwd_flops / (bwd_ms / 1e3) / 1e12
     fwd_tf = fwd_flops / (fwd_ms / 1e3) / 1e12
-    roofline = {"kernel": "seqattn_chunk_bwd (Delta prep + bwd_bf16_kernel)", "bound": "tensor",
+    roofline = {"kernel": "seqattn_chunk_bwd (row-statistics pre-pass + bwd_bf16_kernel)", "bound": "tensor",
                 "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak,
                 "peak_source": peak_src,
                 "traffic": BWD_TRAFFIC_BYTES_PER_LAUNCH,
@@ -371,7 +371,7 @@ def run_ours(args, w):
         cpu_baseline = {"value": f / s / 1e12, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
                         "sample": desc, "seconds": s}
 
-    launches_per_step = 1 + D + 2 * D   # reset, fwd per chunk, (Delta prep + bwd) per chunk
+    launches_per_step = 1 + D + 2 * D   # reset, fwd per chunk, (statistics pre-pass + bwd) per chunk
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,

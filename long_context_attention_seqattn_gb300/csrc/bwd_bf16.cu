@@ -32,8 +32,9 @@
 //   warp 1       TMEM owner + MMA issuer of S^T = K Q^T (M=128 keys, N=64, SS)
 //   warp 15      MMA issuer of dP^T = V dO^T (M=128 keys, N=64, SS)
 //   warp 14      MMA issuer of dV += P^T dO (as soon as P^T is written),
-//                dK += dS^T Q (M=128, N=128, K=64; A from TMEM) and
-//                dQ^T = K^T dS^T (M=128 d, N=64, K=128; SS)
+//                dK += dS^T Q (M=128, N=d, K=64; A from TMEM) and
+//                dQ^T = K^T dS^T (M=128 rows of d, zero-padded when d = 64;
+//                N=64, K=128; SS)
 //   warps 2..9   P^T, then dS^T: two warps per TMEM lane quadrant, 32 query
 //                columns each; dS^T also to shared memory for dQ^T; the final
 //                dK (warps 2-5) / dV (6-9) read-modify-write

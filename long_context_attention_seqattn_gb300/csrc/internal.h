@@ -41,7 +41,7 @@ cudaError_t launch_scale_rows_f32(float* a, float* b, int B, int64_t T, int64_t 
                                   int64_t row_floats, float scale, cudaStream_t s);
 
 // ---- bf16 tensor-core path (TMA + tcgen05 + TMEM) -------------------------
-// Tensor maps are built by the front end (see tma_maps in seqattn_api.cu).
+// Tensor maps are built by the front end (make_map in seqattn_api.cu).
 struct Bf16FwdMaps {
   CUtensorMap q, k, v;
 };

@@ -1,6 +1,7 @@
 // seqattn_api.cu -- the C ABI declared in include/seqattn.h: argument
-// validation (before any launch), TMA tensor maps, the per-device error word
-// and dispatch to the float32 and bf16 kernel families.
+// validation (before any launch), TMA tensor maps, the per-device error word,
+// and dispatch to the float32 and bf16 kernel families, the accumulator row
+// scaling and the projection weight gradient.
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <stdarg.h>
