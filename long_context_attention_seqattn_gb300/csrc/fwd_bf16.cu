@@ -6,8 +6,9 @@
 // Eqs. (12)-(14) named in its "Circularity Check"; the stored row statistic
 // M^(i) of the StreamBP verdict page's stored-activation list).
 //
-// One CTA owns one 128-row query tile of one head and streams the head's
-// key/value tiles [kv_begin, q0 + 128) through shared memory:
+// One CTA owns one 128-row query tile of one head (head dim D = 64 or 128,
+// a template parameter) and streams the head's key/value tiles
+// [kv_begin, min(q0 + 128, q_end)) through shared memory:
 //   warp 0      TMA producer of Q (once) and K tiles (3-stage ring)
 //   warp 10     TMA producer of V tiles (its own 3-stage ring, so a K load
 //               never queues behind a V slot that frees later)

@@ -1,7 +1,8 @@
 // simt_f32.cu -- the float32 path of the chunk calls (plain FMA arithmetic,
 // no tensor cores, so results stay within float32 rounding of the exact
 // value), the Delta preprocess of that path, the row-statistics pre-pass of
-// the bf16 tensor-core backward, and the accumulator zero fill.
+// the bf16 tensor-core backward, the accumulator zero fill and SpaCO's
+// accumulator row scaling.
 //
 // Operation: the partitioned causal attention of the StreamBP review page
 // (Property 3.1 and Eqs. (12)-(14) named in its "Circularity Check"):
