@@ -36,14 +36,17 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-def test_noalloc_backward_matches_workspace_backward(dtype):
+@pytest.mark.parametrize("dtype,q_start,c,d", [
+    ("bf16", 256, 512, 128),
+    ("fp32", 256, 512, 128),
+    ("bf16", 200, 300, 64),      # chunk off the tile grid, partial last query tile, head_dim 64
+])
+def test_noalloc_backward_matches_workspace_backward(dtype, q_start, c, d):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     build.build()
     lib = binding.load_library()
-    B, T, Hq, Hkv, d = 1, 768, 4, 2, 128
-    q_start, c = 256, 512
+    B, T, Hq, Hkv = 1, 768, 4, 2
     dt = inputs.torch_dtype(dtype)
     q, k, v, do = (inputs.draw(n, 77, B, T, h, d, dt).cuda()
                    for n, h in (("q", Hq), ("k", Hkv), ("v", Hkv), ("do", Hq)))
