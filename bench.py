@@ -33,7 +33,7 @@ FALLBACK_SUSTAINED_TFLOPS = 1700.0   # used only when no measured peaks file exi
 # DRAM traffic (bytes read + written) per backward launch, from the ncu
 # launch list of the bench workload (average over its 16 chunk launches);
 # set to None whenever the kernel changes until it is measured again.
-BWD_TRAFFIC_BYTES_PER_LAUNCH = 466.3e6   # bwd_bf16_kernel<128>, prefix tiles first per head, diagonal tiles last
+BWD_TRAFFIC_BYTES_PER_LAUNCH = 463.8e6   # bwd_bf16_kernel<128>, prefix tiles first per head, dK/dV by fp32 reductions
 
 
 def parse_args():
@@ -215,6 +215,7 @@ def run_ours(args, w):
 
     main = torch.cuda.current_stream()
     n_fwd = binding.auto_fwd_streams(q, c)
+    n_bwd = binding.auto_bwd_streams(q, k, c)
     sides = binding.side_streams(dev, n_fwd - 1)
 
     def step(events=None):
@@ -233,15 +234,11 @@ def run_ours(args, w):
             main.wait_stream(sd)
         if events is not None:
             events["fwd"][1].record(main)
-        for i in range(D - 1, -1, -1):
-            s = starts[i]
-            e = min(s + c, T)
-            if events is not None:
-                events["bwd"][i][0].record()
-            binding.chunk_bwd(q[:, s:e], k, v, bufs.o[:, s:e], bufs.lse_chunks[i], do[:, s:e],
-                              bufs.dq[:, s:e], bufs.dk, bufs.dv, s, workspace=bufs.workspace)
-            if events is not None:
-                events["bwd"][i][1].record()
+        # chunk backwards D-1..0 over n_bwd streams (binding.backward_chunks),
+        # timed as a phase from the fork to the join
+        binding.backward_chunks(q, k, v, do, c, bufs, None, main, n_bwd)
+        if events is not None:
+            events["bwd"][1].record(main)
 
     if (T % c) != 0 or w.batch != 1:
         raise SystemExit("bench expects B=1 and T divisible by the chunk")
@@ -253,7 +250,7 @@ def run_ours(args, w):
     def ev():
         return torch.cuda.Event(enable_timing=True)
 
-    launch_ev = [{"fwd": (ev(), ev()), "bwd": [(ev(), ev()) for _ in range(D)]} for _ in range(args.steps)]
+    launch_ev = [{"fwd": (ev(), ev()), "bwd": (None, ev())} for _ in range(args.steps)]
     gpu_id = None
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -280,7 +277,7 @@ def run_ours(args, w):
 
     # per-launch roofline (live CUDA-event durations inside the timed region)
     fwd_ms = sum(e["fwd"][0].elapsed_time(e["fwd"][1]) for e in launch_ev)
-    bwd_ms = sum(a.elapsed_time(b) for e in launch_ev for a, b in e["bwd"])
+    bwd_ms = sum(e["fwd"][1].elapsed_time(e["bwd"][1]) for e in launch_ev)
     pairs = sum(workloads.causal_pairs(s, min(c, T - s)) for s in starts)
     fwd_flops = 4 * w.batch * w.hq * w.head_dim * pairs * args.steps
     bwd_flops = 10 * w.batch * w.hq * w.head_dim * pairs * args.steps
@@ -291,7 +288,10 @@ def run_ours(args, w):
                 "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak,
                 "peak_source": peak_src,
                 "traffic": BWD_TRAFFIC_BYTES_PER_LAUNCH,
-                "per_launch": f"causal bwd FLOPs 10*Hq*d*pairs(chunk) averaged over {D} launches/step",
+                "per_launch": f"causal bwd FLOPs 10*Hq*d*pairs(chunk) over the {D} chunk backwards of a "
+                              f"step, timed as a phase ({n_bwd} stream(s), fork to join); avg_launch_ms is "
+                              f"the phase divided by {D}",
+                "bwd_streams": n_bwd,
                 "avg_launch_ms": bwd_ms / (D * args.steps)}
     roofline_fwd = {"kernel": "seqattn_chunk_fwd (fwd_bf16_kernel)", "bound": "tensor", "achieved": fwd_tf,
                     "peak": peak, "unit": "TFLOP/s", "frac": fwd_tf / peak,

@@ -255,6 +255,14 @@ class LayerBuffers:
                            for s in self.starts]
         self.workspace = torch.empty(max(256, bwd_workspace_size(k, Hq, chunk, q.dtype)),
                                      dtype=torch.uint8, device=dev)
+        self.workspaces = [self.workspace]
+
+    def workspace_for(self, j):
+        """Backward workspace of stream ``j`` (backward calls that may run at
+        the same time need one each)."""
+        while len(self.workspaces) <= j:
+            self.workspaces.append(torch.empty_like(self.workspace))
+        return self.workspaces[j]
 
 
 def _rows(t, s, e):
@@ -304,11 +312,13 @@ def forward_chunks(q, k, v, chunk, bufs, scale=None, stream=None, fwd_streams=No
     for i, s in enumerate(bufs.starts):
         e = min(s + chunk, T)
         st = main if i % fwd_streams == 0 else sides[i % fwd_streams - 1]
-        o_c = bufs.o[:, s:e]
-        if o_c.is_contiguous():
-            chunk_fwd(_rows(q, s, e), k, v, o_c, bufs.lse_chunks[i], s, s, scale, st)
-        else:
-            with torch.cuda.stream(st):
+        # the row gathers of a batched chunk (B > 1) and their temporaries
+        # belong to the chunk's own stream
+        with torch.cuda.stream(st):
+            o_c = bufs.o[:, s:e]
+            if o_c.is_contiguous():
+                chunk_fwd(_rows(q, s, e), k, v, o_c, bufs.lse_chunks[i], s, s, scale, st)
+            else:
                 tmp = torch.empty_like(o_c.contiguous())
                 chunk_fwd(_rows(q, s, e), k, v, tmp, bufs.lse_chunks[i], s, s, scale, st)
                 o_c.copy_(tmp)
@@ -316,19 +326,103 @@ def forward_chunks(q, k, v, chunk, bufs, scale=None, stream=None, fwd_streams=No
         main.wait_stream(sd)
 
 
+def auto_bwd_streams(q, k, chunk):
+    """Streams for the chunk backwards.  bf16 backward calls add into the
+    accumulators atomically and may overlap, which pays when the chunk grids
+    (128-key tiles of the prefix x key/value heads x batch CTAs) are short:
+    one chunk's last wave, its statistics pre-pass and the launch boundaries
+    then overlap the next chunk's work.  Measured on a 16384-token layer
+    (backward TFLOP/s, 1 / 2 / 4 streams): chunk 128: 484 / 567 / 606, 512:
+    878 / 974 / 1005, 2048: 1128 / 1160, 4096: 1238 / 1240; on a 32768-token
+    layer at chunk 2048 (grids of 7 waves on average) one stream is faster,
+    1171 against 1129.  So: one stream when the average chunk grid fills four
+    waves of the SMs; otherwise four streams for chunks of at most 512 rows
+    (a CTA runs only G ceil(c/64) short steps) and two above.  float32 calls
+    update the accumulators with plain read-modify-writes and always take
+    one stream."""
+    if q.dtype != torch.bfloat16:
+        return 1
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    starts = list(range(0, T, chunk))
+    tiles = sum(-(-min(s + chunk, T) // 128) for s in starts) / len(starts)
+    sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+    if tiles * Hkv * B >= 4 * sms:
+        return 1
+    return 4 if chunk <= 512 else 2
+
+
+def backward_chunks(q, k, v, d_o, chunk, bufs, scale=None, stream=None, bwd_streams=None,
+                    bwd_order="descending", on_final=None, before_chunk=None):
+    """Backward every chunk of ``bufs`` (after ``forward_chunks``): dQ rows
+    overwritten, dK/dV added into the running sums.  The k-th chunk in
+    ``bwd_order`` runs on stream k % bwd_streams (``stream`` and side streams
+    forked from it), each stream with its own workspace; ``bwd_streams``
+    defaults to ``auto_bwd_streams``.
+
+    ``on_final(i, s, e, events)`` (descending order only) is called after
+    chunk i's backward is enqueued: once every CUDA event in ``events`` has
+    completed, dQ rows [s, e) and the dK/dV rows [s, e) are final -- every
+    chunk from i on has added its share (SeCO's relay).
+    ``before_chunk(i, st)`` is called before chunk i's backward is enqueued
+    on stream ``st`` (to make it wait for that chunk's inputs).  All streams
+    are joined back into ``stream`` before returning."""
+    B, T, Hq, d = q.shape
+    if bwd_streams is None:
+        bwd_streams = auto_bwd_streams(q, k, chunk)
+    if bwd_streams > 1 and q.dtype != torch.bfloat16:
+        raise ValueError("overlapping backward calls need the bf16 path (atomic accumulator updates)")
+    if on_final is not None and bwd_order != "descending":
+        raise ValueError("rows become final only in the last-to-first relay order")
+    main = stream if stream is not None else torch.cuda.current_stream()
+    sides = side_streams(q.device, bwd_streams - 1)
+    for sd in sides:
+        sd.wait_stream(main)
+    order = list(enumerate(bufs.starts))
+    if bwd_order == "descending":
+        order = order[::-1]
+    last = [None] * bwd_streams            # event after each stream's latest chunk
+    for n, (i, s) in enumerate(order):
+        e = min(s + chunk, T)
+        j = n % bwd_streams
+        st = main if j == 0 else sides[j - 1]
+        if before_chunk is not None:
+            before_chunk(i, st)
+        with torch.cuda.stream(st):                # as in forward_chunks
+            dq_c = bufs.dq[:, s:e]
+            tgt = dq_c if dq_c.is_contiguous() else torch.empty_like(dq_c.contiguous())
+            chunk_bwd(_rows(q, s, e), k, v, _rows(bufs.o, s, e), bufs.lse_chunks[i], _rows(d_o, s, e),
+                      tgt, bufs.dk, bufs.dv, s, s, scale, bufs.workspace_for(j), st)
+            if tgt is not dq_c:
+                dq_c.copy_(tgt)
+        if on_final is not None or bwd_streams > 1:
+            ev = torch.cuda.Event()
+            ev.record(st)
+            last[j] = ev
+        if on_final is not None:
+            # chunks i+1 .. i+bwd_streams-1 were each the latest on one of
+            # the other streams; every earlier chunk ran before one of them
+            on_final(i, s, e, [x for x in last if x is not None])
+    for sd in sides:
+        main.wait_stream(sd)
+
+
 def layer_forward_backward(q, k, v, d_o, chunk, scale=None, bufs=None, stream=None,
-                           bwd_order="descending", fwd_streams=None, wgrad=None):
+                           bwd_order="descending", fwd_streams=None, wgrad=None, bwd_streams=None):
     """One pass of the chunked layer: reset the running sums, forward chunks
     0..D-1 (over ``fwd_streams`` streams, see ``forward_chunks``), backward
-    chunks D-1..0 (SeCO's last-to-first relay order).  Returns the
-    LayerBuffers holding O, per-chunk LSE, dQ, dK, dV.
+    chunks D-1..0 (SeCO's last-to-first relay order; over ``bwd_streams``
+    streams, see ``backward_chunks``).  Returns the LayerBuffers holding O,
+    per-chunk LSE, dQ, dK, dV.
 
     ``wgrad = (h, dw_q, dw_k, dw_v)`` also runs the projections' weight
     gradients in the relay: right after chunk i's backward, its dQ rows and
     its dK/dV rows are final (every later chunk has run), so
     dw_x += H^(i)T dX^(i) is added for each of the three (h: [B, T, d_model]
     bf16; dw_q: [d_model, Hq d], dw_k, dw_v: [d_model, Hkv d], float32,
-    accumulated).  Needs the descending order."""
+    accumulated).  Needs the descending order.  With more than one backward
+    stream they run on a relay stream that waits until each chunk's rows are
+    final."""
     B, T, Hq, d = q.shape
     if bufs is None:
         bufs = LayerBuffers(q, k, chunk)
@@ -336,24 +430,28 @@ def layer_forward_backward(q, k, v, d_o, chunk, scale=None, bufs=None, stream=No
         raise ValueError("the projection gradients run in the last-to-first relay order")
     reset_accum(bufs.dk, bufs.dv, Hq, stream)
     forward_chunks(q, k, v, chunk, bufs, scale, stream, fwd_streams)
-    order = list(enumerate(bufs.starts))
-    if bwd_order == "descending":
-        order = order[::-1]
-    ws = None
+    if bwd_streams is None:
+        bwd_streams = auto_bwd_streams(q, k, chunk)
+    main = stream if stream is not None else torch.cuda.current_stream()
+    on_final = None
+    relay = main
     if wgrad is not None:
         ws = torch.empty(wgrad_workspace_size(B, chunk, Hq * d), dtype=torch.uint8, device=q.device)
-    for i, s in order:
-        e = min(s + chunk, T)
-        dq_c = bufs.dq[:, s:e]
-        tgt = dq_c if dq_c.is_contiguous() else torch.empty_like(dq_c.contiguous())
-        chunk_bwd(_rows(q, s, e), k, v, _rows(bufs.o, s, e), bufs.lse_chunks[i], _rows(d_o, s, e),
-                  tgt, bufs.dk, bufs.dv, s, s, scale, bufs.workspace, stream)
-        if tgt is not dq_c:
-            dq_c.copy_(tgt)
-        if wgrad is not None:
+        if bwd_streams > 1:
+            relay = side_streams(q.device, bwd_streams)[bwd_streams - 1]
+            relay.wait_stream(main)
+
+        def on_final(i, s, e, events):
             h, dw_q, dw_k, dw_v = wgrad
+            if relay is not main:
+                for ev in events:
+                    relay.wait_event(ev)
             for g, dw in ((bufs.dq, dw_q), (bufs.dk, dw_k), (bufs.dv, dw_v)):
-                proj_wgrad(h, g, dw, s, e, ws, stream)
+                proj_wgrad(h, g, dw, s, e, ws, relay)
+
+    backward_chunks(q, k, v, d_o, chunk, bufs, scale, main, bwd_streams, bwd_order, on_final)
+    if relay is not main:
+        main.wait_stream(relay)
     return bufs
 
 
@@ -382,21 +480,25 @@ def spaco_layer_forward_backward(q, k, v, d_o, chunk, selected, factor=None, sca
         raise ValueError(f"selected chunk indices must lie in [0, {n_chunks})")
     if factor is None:
         factor = spaco_factor(n_chunks, len(chosen))
-    reset_accum(bufs.dk, bufs.dv, Hq, stream)
-    forward_chunks(q, k, v, chunk, bufs, scale, stream)
-    for i, s in reversed(list(enumerate(bufs.starts))):
-        e = min(s + chunk, T)
-        dq_c = bufs.dq[:, s:e]
-        if i not in chosen:
-            scale_accum_rows(bufs.dk, bufs.dv, s, e, 0.0, stream)
-            scale_accum_rows(bufs.dq, bufs.dq, s, e, 0.0, stream)   # no dQ for this chunk
-            continue
-        scale_accum_rows(bufs.dk, bufs.dv, s, e, factor, stream)
-        tgt = dq_c if dq_c.is_contiguous() else torch.empty_like(dq_c.contiguous())
-        chunk_bwd(_rows(q, s, e), k, v, _rows(bufs.o, s, e), bufs.lse_chunks[i], _rows(d_o, s, e),
-                  tgt, bufs.dk, bufs.dv, s, s, scale, bufs.workspace, stream)
-        if tgt is not dq_c:
-            dq_c.copy_(tgt)
+    main = stream if stream is not None else torch.cuda.current_stream()
+    reset_accum(bufs.dk, bufs.dv, Hq, main)
+    forward_chunks(q, k, v, chunk, bufs, scale, main)
+    # one stream: each selected chunk's scaling must follow every later
+    # chunk's additions into its rows
+    with torch.cuda.stream(main):
+        for i, s in reversed(list(enumerate(bufs.starts))):
+            e = min(s + chunk, T)
+            dq_c = bufs.dq[:, s:e]
+            if i not in chosen:
+                scale_accum_rows(bufs.dk, bufs.dv, s, e, 0.0, main)
+                scale_accum_rows(bufs.dq, bufs.dq, s, e, 0.0, main)   # no dQ for this chunk
+                continue
+            scale_accum_rows(bufs.dk, bufs.dv, s, e, factor, main)
+            tgt = dq_c if dq_c.is_contiguous() else torch.empty_like(dq_c.contiguous())
+            chunk_bwd(_rows(q, s, e), k, v, _rows(bufs.o, s, e), bufs.lse_chunks[i], _rows(d_o, s, e),
+                      tgt, bufs.dk, bufs.dv, s, s, scale, bufs.workspace, main)
+            if tgt is not dq_c:
+                dq_c.copy_(tgt)
     return bufs
 
 
@@ -459,6 +561,7 @@ class HostLayerPass:
         self.h_dv = torch.empty(h_k.shape, dtype=torch.float32, pin_memory=True)
         self.up = torch.cuda.Stream()
         self.down = torch.cuda.Stream()
+        self.bwd_streams = auto_bwd_streams(self.d_in[0], self.d_in[1], chunk)
 
     def bytes_moved(self):
         h2d = sum(x.numel() * x.element_size() for x in self.h_in)
@@ -477,7 +580,7 @@ class HostLayerPass:
         starts = b.starts
         self.up.wait_stream(main)
         self.down.wait_stream(main)
-        ev_in, ev_do = [], []
+        ev_in = []
         with torch.cuda.stream(self.up):
             for s in starts:
                 e = min(s + c, T)
@@ -486,12 +589,16 @@ class HostLayerPass:
                 ev = torch.cuda.Event()
                 ev.record(self.up)
                 ev_in.append(ev)
-            for s in starts:
+            # dO in the backward's (last-to-first) order, so that the first
+            # backward call waits only for its own chunk
+            ev_do = [None] * len(starts)
+            for i in range(len(starts) - 1, -1, -1):
+                s = starts[i]
                 e = min(s + c, T)
                 do[:, s:e].copy_(h_do[:, s:e], non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(self.up)
-                ev_do.append(ev)
+                ev_do[i] = ev
         reset_accum(b.dk, b.dv, q.shape[2], main)
         # chunk forwards alternate over two compute streams (see forward_chunks)
         side = side_streams(q.device, 1)[0]
@@ -508,21 +615,21 @@ class HostLayerPass:
                 self.h_o[:, s:e].copy_(b.o[:, s:e], non_blocking=True)
                 self.h_lse[i].copy_(b.lse_chunks[i], non_blocking=True)
         main.wait_stream(side)
-        for i in range(len(starts) - 1, -1, -1):
-            s = starts[i]
-            e = min(s + c, T)
-            main.wait_event(ev_do[i])
-            chunk_bwd(_rows(q, s, e), k, v, _rows(b.o, s, e), b.lse_chunks[i], _rows(do, s, e),
-                      b.dq[:, s:e], b.dk, b.dv, s, s, None, b.workspace, main)
-            ev = torch.cuda.Event()
-            ev.record(main)
-            self.down.wait_event(ev)
+
+        def before_chunk(i, st):
+            st.wait_event(ev_do[i])
+
+        def on_final(i, s, e, events):
+            # rows of chunk i are final: later chunks and this one were the
+            # only ones touching them
+            for ev in events:
+                self.down.wait_event(ev)
             with torch.cuda.stream(self.down):
-                # rows of chunk i are final: later chunks (already done) and
-                # this one were the only ones touching them
                 self.h_dq[:, s:e].copy_(b.dq[:, s:e], non_blocking=True)
                 self.h_dk[:, s:e].copy_(b.dk[:, s:e], non_blocking=True)
                 self.h_dv[:, s:e].copy_(b.dv[:, s:e], non_blocking=True)
+
+        backward_chunks(q, k, v, do, c, b, None, main, self.bwd_streams, "descending", on_final, before_chunk)
         main.wait_stream(self.down)
         main.wait_stream(self.up)
         return self.h_o, self.h_lse, self.h_dq, self.h_dk, self.h_dv

@@ -12,10 +12,12 @@
 // One CTA owns one 128-key tile of one key/value head: it loops over the G
 // query heads of the group and the chunk's 64-row query tiles that can see the
 // tile ("steps"), keeps dK and dV for its 128 keys in TMEM for the whole loop,
-// and finally adds them into the float32 accumulators with a plain
-// read-modify-write (no other CTA touches those rows in this call, so there is
-// no atomic contention across query tiles).  dQ partial products of every key
-// tile are summed into the zeroed dq with fp32 reductions.  Chunks may start
+// and finally adds them into the float32 accumulators with vector fp32
+// reductions (16-byte atomic adds carried out in L2).  Within one call no other
+// CTA touches those rows, so the reductions meet no contention; they need no
+// load of the old sums, and backward calls of different chunks may run
+// concurrently on different streams.  dQ partial products of every key tile
+// are summed into the zeroed dq with fp32 reductions.  Chunks may start
 // and end anywhere: a partial last query tile reads padding statistics
 // (-inf, 0) that make its extra rows' P exactly 0, and rows past the chunk
 // are never stored.
@@ -37,7 +39,7 @@
 //                N=64, K=128; SS)
 //   warps 2..9   P^T, then dS^T: two warps per TMEM lane quadrant, 32 query
 //                columns each; dS^T also to shared memory for dQ^T; the final
-//                dK (warps 2-5) / dV (6-9) read-modify-write
+//                dK (warps 2-5) / dV (6-9) reductions
 //   warps 10..13 dQ^T from TMEM -> fp32 reductions into dq
 // Three issuing threads because one thread keeps only about one tcgen05.mma
 // in flight per ~90 cycles, whatever its shape; S^T and dP^T, which gate the
@@ -474,23 +476,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_base + col + c0 + 32, r1);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32 && store; j += 4) {
-          float4 a = dst[(c0 + j) / 4];
-          a.x += f * __uint_as_float(r0[j]);
-          a.y += f * __uint_as_float(r0[j + 1]);
-          a.z += f * __uint_as_float(r0[j + 2]);
-          a.w += f * __uint_as_float(r0[j + 3]);
-          dst[(c0 + j) / 4] = a;
-        }
+        for (int j = 0; j < 32 && store; j += 4)
+          atomicAdd(dst + (c0 + j) / 4, make_float4(f * __uint_as_float(r0[j]), f * __uint_as_float(r0[j + 1]),
+                                                    f * __uint_as_float(r0[j + 2]), f * __uint_as_float(r0[j + 3])));
 #pragma unroll
-        for (int j = 0; j < 32 && store; j += 4) {
-          float4 a = dst[(c0 + 32 + j) / 4];
-          a.x += f * __uint_as_float(r1[j]);
-          a.y += f * __uint_as_float(r1[j + 1]);
-          a.z += f * __uint_as_float(r1[j + 2]);
-          a.w += f * __uint_as_float(r1[j + 3]);
-          dst[(c0 + 32 + j) / 4] = a;
-        }
+        for (int j = 0; j < 32 && store; j += 4)
+          atomicAdd(dst + (c0 + 32 + j) / 4,
+                    make_float4(f * __uint_as_float(r1[j]), f * __uint_as_float(r1[j + 1]),
+                                f * __uint_as_float(r1[j + 2]), f * __uint_as_float(r1[j + 3])));
       }
     }
   } else {
