@@ -31,9 +31,13 @@ UNIT = "TFLOP/s"
 FALLBACK_SUSTAINED_TFLOPS = 1700.0   # used only when no measured peaks file exists
 
 # DRAM traffic (bytes read + written) per backward launch, from the ncu
-# launch list of the bench workload (average over its 16 chunk launches);
-# set to None whenever the kernel changes until it is measured again.
-BWD_TRAFFIC_BYTES_PER_LAUNCH = 463.8e6   # bwd_bf16_kernel<128>, prefix tiles first per head, dK/dV by fp32 reductions
+# launch list of a workload (average over its chunk launches), keyed by the
+# workload; other workloads report None, and an entry is removed whenever
+# the kernel changes until it is measured again.
+BWD_TRAFFIC_BYTES_PER_LAUNCH = {
+    # bwd_bf16_kernel<128>, prefix tiles first per head, dK/dV by fp32 reductions
+    "llama3-8b-layer-t32768-c2048": 463.8e6,
+}
 
 
 def parse_args():
@@ -287,7 +291,7 @@ def run_ours(args, w):
     roofline = {"kernel": "seqattn_chunk_bwd (row-statistics pre-pass + bwd_bf16_kernel)", "bound": "tensor",
                 "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak,
                 "peak_source": peak_src,
-                "traffic": BWD_TRAFFIC_BYTES_PER_LAUNCH,
+                "traffic": BWD_TRAFFIC_BYTES_PER_LAUNCH.get(w.name),
                 "per_launch": f"causal bwd FLOPs 10*Hq*d*pairs(chunk) over the {D} chunk backwards of a "
                               f"step, timed as a phase ({n_bwd} stream(s), fork to join); avg_launch_ms is "
                               f"the phase divided by {D}",

@@ -340,14 +340,20 @@ def auto_bwd_streams(q, k, chunk):
     (a CTA runs only G ceil(c/64) short steps) and two above.  float32 calls
     update the accumulators with plain read-modify-writes and always take
     one stream."""
+    B, T, Hq, d = q.shape
     if q.dtype != torch.bfloat16:
         return 1
-    B, T, Hq, d = q.shape
-    Hkv = k.shape[2]
-    starts = list(range(0, T, chunk))
-    tiles = sum(-(-min(s + chunk, T) // 128) for s in starts) / len(starts)
     sms = torch.cuda.get_device_properties(q.device).multi_processor_count
-    if tiles * Hkv * B >= 4 * sms:
+    return bwd_streams_for(B, T, k.shape[2], chunk, True, sms)
+
+
+def bwd_streams_for(batch, seq_len, num_kv_heads, chunk, bf16, sms):
+    """The rule of ``auto_bwd_streams`` on plain numbers (host logic only)."""
+    if not bf16:
+        return 1
+    starts = range(0, seq_len, chunk)
+    tiles = sum(-(-min(s + chunk, seq_len) // 128) for s in starts) / len(starts)
+    if tiles * num_kv_heads * batch >= 4 * sms:
         return 1
     return 4 if chunk <= 512 else 2
 

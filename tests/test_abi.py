@@ -161,3 +161,35 @@ def test_bwd_validation(lib):
 def test_reset_validation(lib):
     assert lib.seqattn_reset_accum(ctypes.byref(_pb()), NUL, P, NUL) == 1
     assert lib.seqattn_reset_accum(None, P, P, NUL) == 1
+
+
+# ------------------------------------------------------------------ host logic: backward streams
+
+@pytest.mark.parametrize("B,T,Hkv,chunk,bf16,want", [
+    (1, 32768, 8, 2048, True, 1),      # grids of about 7 waves: one stream
+    (1, 131072, 8, 4096, True, 1),
+    (1, 8192, 8, 512, True, 4),        # short grids, short CTAs
+    (1, 16384, 8, 128, True, 4),
+    (1, 16384, 8, 512, True, 4),
+    (1, 16384, 8, 1024, True, 2),
+    (1, 16384, 8, 2048, True, 2),      # 576 CTAs on average, under four waves of 152
+    (1, 16384, 8, 4096, True, 1),      # 640 on average
+    (1, 16384, 8, 16384, True, 1),
+    (1, 512, 2, 128, False, 1),        # float32: plain read-modify-writes, one stream
+])
+def test_backward_stream_rule(B, T, Hkv, chunk, bf16, want):
+    assert binding.bwd_streams_for(B, T, Hkv, chunk, bf16, 152) == want
+
+
+def test_backward_chunks_guards():
+    """Overlapping backward calls need the bf16 path's atomic updates, and
+    rows become final only in the last-to-first order; both are refused
+    before any launch."""
+    import torch
+    q32 = torch.zeros((1, 256, 2, 64), dtype=torch.float32)
+    with pytest.raises(ValueError, match="bf16"):
+        binding.backward_chunks(q32, q32, q32, q32, 128, None, bwd_streams=2)
+    q16 = torch.zeros((1, 256, 2, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="relay"):
+        binding.backward_chunks(q16, q16, q16, q16, 128, None, bwd_streams=1, bwd_order="ascending",
+                                on_final=lambda *a: None)

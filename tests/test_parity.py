@@ -317,24 +317,49 @@ def test_proj_wgrad_accumulates_h_transpose_g():
     assert_wgrad("dW", cpu64(dw), ref)
 
 
-@pytest.mark.parametrize("B,T,Hq,Hkv,d,dm,chunk", [
-    (1, 512, 4, 2, 128, 256, 128),
-    (2, 300, 4, 1, 64, 64, 100),       # ragged last chunk, d = 64, batch 2
+@pytest.mark.parametrize("B,T,Hq,Hkv,d,dm,chunk,streams", [
+    (1, 512, 4, 2, 128, 256, 128, None),
+    (1, 512, 4, 2, 128, 256, 128, 1),
+    (2, 300, 4, 1, 64, 64, 100, None),  # ragged last chunk, d = 64, batch 2
+    (2, 300, 4, 1, 64, 64, 100, 3),
 ])
-def test_layer_pass_with_projection_wgrad(B, T, Hq, Hkv, d, dm, chunk):
+def test_layer_pass_with_projection_wgrad(B, T, Hq, Hkv, d, dm, chunk, streams):
     """The relay pass with the projections' weight gradients: after chunk i's
     backward, dW_q, dW_k, dW_v += H^(i)T (dQ, dK, dV rows of chunk i).  The
-    sum over chunks equals the oracle's H^T dQ, H^T dK, H^T dV."""
+    sum over chunks equals the oracle's H^T dQ, H^T dK, H^T dV, also with the
+    chunk backwards spread over several streams (each chunk's weight
+    gradients then wait until every stream has passed every later chunk)."""
     cpu = small_inputs(B, T, Hq, Hkv, d, "bf16", 88)
     h = inputs.draw("h", 88, B, T, 1, dm, torch.bfloat16)[:, :, 0]
     dws = [torch.zeros((dm, n), device="cuda") for n in (Hq * d, Hkv * d, Hkv * d)]
     bufs = binding.layer_forward_backward(*[x.cuda() for x in cpu], chunk,
-                                          wgrad=(h.cuda().contiguous(), *dws))
+                                          wgrad=(h.cuda().contiguous(), *dws), bwd_streams=streams)
     binding.sync_status()
     _, _, dq, dk, dv = oracle.chunked_layer(*(x.to(torch.float64).numpy() for x in cpu), chunk, d ** -0.5)
     hn = h.double().numpy()
     for name, got, g in zip(("dW_q", "dW_k", "dW_v"), dws, (dq, dk, dv)):
         assert_wgrad(name, cpu64(got), oracle.projection_wgrad(hn, g))
+
+
+@pytest.mark.parametrize("streams", [2, 4])
+def test_bf16_backward_streams_match_one_stream(streams):
+    """Chunk backwards spread over several streams (their dK/dV reductions
+    meeting in L2) give the one-stream pass up to the order of the fp32
+    additions, and both match the oracle."""
+    B, T, Hq, Hkv, d, chunk = 2, 700, 4, 2, 128, 128   # batch 2, ragged last chunk
+    cpu = small_inputs(B, T, Hq, Hkv, d, "bf16", 77)
+    dev = [x.cuda() for x in cpu]
+    one = binding.layer_forward_backward(*dev, chunk, bwd_streams=1)
+    ref = [x.clone() for x in (one.dq, one.dk, one.dv)]
+    many = binding.layer_forward_backward(*dev, chunk, bwd_streams=streams)
+    binding.sync_status()
+    for name, a, r in zip(("dQ", "dK", "dV"), (many.dq, many.dk, many.dv), ref):
+        a, r = cpu64(a), cpu64(r)
+        rel = np.linalg.norm(a - r) / np.linalg.norm(r)
+        assert rel <= 1e-5, f"{name}: {streams}-stream vs one-stream rel-L2 {rel:.2e}"
+    _, _, dq, dk, dv = oracle.chunked_layer(*(x.to(torch.float64).numpy() for x in cpu), chunk, d ** -0.5)
+    for name, a, r in zip(("dQ", "dK", "dV"), (many.dq, many.dk, many.dv), (dq, dk, dv)):
+        assert_bf16(f"{streams} streams {name}", cpu64(a), r)
 
 
 def test_bf16_qwen3_4b_layer_two_groups():
