@@ -7,7 +7,7 @@ Metric: causal fwd+bwd TFLOP/s (14 * B * Hq * d * T(T+1)/2 FLOPs credited per
 pass).  One JSON line on stdout (rank 0).  Usage:
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference]
+                    [--impl ours|reference] [--oracle-threads N]
 
 With N > 1 it is launched by torchrun, one process per GPU; every rank runs
 its own independent problems (weak scaling, no data-path collective) and the
@@ -50,6 +50,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-wgrad", action="store_true")
+    ap.add_argument("--oracle-threads", type=int, default=None,
+                    help="BLAS threads of the float64 oracle (cpu_baseline and --impl reference); "
+                         "default: every core of the process's affinity mask")
     return ap.parse_args()
 
 
@@ -149,11 +152,17 @@ def oracle_sample(w, seed, heads):
     return flops, secs, desc
 
 
+ORACLE_THREADS = None   # set from --oracle-threads before NumPy is imported
+
+
 def host_cores():
+    """Threads the oracle's BLAS may use: the affinity mask's cores, or fewer
+    when --oracle-threads caps them."""
     try:
-        return len(os.sched_getaffinity(0))
+        n = len(os.sched_getaffinity(0))
     except AttributeError:
-        return os.cpu_count() or 1
+        n = os.cpu_count() or 1
+    return min(n, ORACLE_THREADS) if ORACLE_THREADS else n
 
 
 # ------------------------------------------------------------------ reference arm
@@ -441,6 +450,12 @@ def run_sweep(args, w):
 
 def main():
     args = parse_args()
+    if args.oracle_threads:
+        # before the first NumPy import: the BLAS thread pool is sized once
+        global ORACLE_THREADS
+        ORACLE_THREADS = args.oracle_threads
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = str(args.oracle_threads)
     from long_context_attention_seqattn_gb300 import workloads
     w = workloads.WORKLOADS[args.workload or workloads.BENCH_WORKLOAD]
     if args.impl == "reference":
