@@ -94,7 +94,7 @@ struct FwdBarriers {
 // All 32 lanes wait; the warp proceeds only if every lane saw the phase, so
 // the warp stays converged for the .sync.aligned tcgen05 instructions.
 __device__ __forceinline__ bool warp_wait(Watchdog& wd, uint64_t* bar, uint32_t parity) {
-  const bool ok = wd.wait(bar, parity);
+  const bool ok = wd.wait_sleep(bar, parity);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = t % kStages;
         const uint32_t ph = (t / kStages) & 1;
         const int krow = b * p.T + p.kv_begin + t * kBN;
-        if (!wd.wait(&empty[st], ph ^ 1)) break;
+        if (!wd.wait_sleep(&empty[st], ph ^ 1)) break;
         mbar_arrive_expect_tx(&full[st], kTileBytes);
 #pragma unroll
         for (int blk = 0; blk < D / 64; ++blk)
@@ -226,11 +226,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int me = (warp == 1) ? 0 : 1;
       bool ok = true;
       if (me == 0) {
-        ok = wd.wait(&bars.q_full, 0);
+        ok = wd.wait_sleep(&bars.q_full, 0);
         for (int t = 0; ok && t < n_kv; ++t) {
           const int ks_st = t % kStages;
-          if (!(ok = wd.wait(&bars.k_full[ks_st], (t / kStages) & 1))) break;
-          if (t >= 2 && !(ok = wd.wait(&bars.pv_done[t & 1], ((t - 2) >> 1) & 1))) break;
+          if (!(ok = wd.wait_sleep(&bars.k_full[ks_st], (t / kStages) & 1))) break;
+          if (t >= 2 && !(ok = wd.wait_sleep(&bars.pv_done[t & 1], ((t - 2) >> 1) & 1))) break;
           tc_fence_after_sync();
           const uint64_t kd = k_desc0 + static_cast<uint64_t>(ks_st * kTileUnits);
 #pragma unroll
@@ -243,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         for (int u = 0; ok && u < n_kv; ++u) {
           const int vs = u % kStages;
-          if (!(ok = wd.wait(&bars.v_full[vs], (u / kStages) & 1))) break;
-          if (!(ok = wd.wait(&bars.p_full[u & 1], (u >> 1) & 1))) break;
+          if (!(ok = wd.wait_sleep(&bars.v_full[vs], (u / kStages) & 1))) break;
+          if (!(ok = wd.wait_sleep(&bars.p_full[u & 1], (u >> 1) & 1))) break;
           tc_fence_after_sync();
           const uint64_t vd = v_desc0 + static_cast<uint64_t>(vs * kTileUnits);
           const uint32_t pa = tmem + kColS + (u & 1) * kBN;   // P in the S buffer, lane 0
@@ -317,18 +317,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = warp_wait(wd, &bars.pv_done[u & 1], (u >> 1) & 1))) break;
           tc_fence_after_sync();
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 64) {
-            uint32_t r0[32], r1[32];
+          for (int c0 = 0; c0 < D; c0 += 32) {   // 32 columns at a time: the scores stay live
+            uint32_t r0[32];
             tmem_ld32(colO + c0, r0);
-            tmem_ld32(colO + c0 + 32, r1);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              r0[j] = __float_as_uint(__uint_as_float(r0[j]) * alpha);
-              r1[j] = __float_as_uint(__uint_as_float(r1[j]) * alpha);
-            }
+            for (int j = 0; j < 32; ++j) r0[j] = __float_as_uint(__uint_as_float(r0[j]) * alpha);
             tmem_st32(colO + c0, r0);
-            tmem_st32(colO + c0 + 32, r1);
           }
           tmem_st_wait();
         }
