@@ -288,7 +288,8 @@ def run_ours(args, w):
     flops_rank = w.causal_flops()
     value = world * flops_rank * args.steps / (ms / 1e3) / 1e12
 
-    # per-launch roofline (live CUDA-event durations inside the timed region)
+    # roofline of both passes, each timed as a phase of every timed step (live
+    # CUDA events on the main stream, from the fork to the join of its streams)
     fwd_ms = sum(e["fwd"][0].elapsed_time(e["fwd"][1]) for e in launch_ev)
     bwd_ms = sum(e["fwd"][1].elapsed_time(e["bwd"][1]) for e in launch_ev)
     pairs = sum(workloads.causal_pairs(s, min(c, T - s)) for s in starts)
