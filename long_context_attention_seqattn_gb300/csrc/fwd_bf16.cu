@@ -330,8 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // P = 2^(s * scale * log2e - m) for this row's 64 keys -> bf16 pairs ->
       // TMEM columns [64h, 64h + 32) of the S buffer (already read above)
-      const uint64_t negm = f2_pack(-m_run, -m_run);
-      const bool live = m_run != -INFINITY;      // a half with no visible key yet writes zeros
+      // a row with no visible key yet (m_run = -inf) has only -inf scores in
+      // this tile: subtracting 0 instead keeps them -inf, and 2^-inf = 0
+      const float m_use = m_run == -INFINITY ? 0.f : m_run;
+      const uint64_t negm = f2_pack(-m_use, -m_use);
       uint64_t lsum = f2_pack(0.f, 0.f);
       uint32_t pw[32];
 #pragma unroll
@@ -340,8 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t x = f2_fma(f2_pack(__uint_as_float(src[0]), __uint_as_float(src[1])), scale2, negm);
         float a, c;
         f2_unpack(x, a, c);
-        const float ea = live ? ex2(a) : 0.f;
-        const float ec = live ? ex2(c) : 0.f;
+        const float ea = ex2(a);
+        const float ec = ex2(c);
         lsum = f2_add(lsum, f2_pack(ea, ec));
         pw[k2] = pack_bf16x2(ea, ec);
       }
