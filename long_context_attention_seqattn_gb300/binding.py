@@ -358,6 +358,24 @@ def bwd_streams_for(batch, seq_len, num_kv_heads, chunk, bf16, sms):
     return 4 if chunk <= 512 else 2
 
 
+def relay_plan(num_chunks, bwd_streams, bwd_order="descending"):
+    """Host plan of ``backward_chunks``: for the n-th call in ``bwd_order``,
+    ``(i, j, after)`` -- chunk i runs on stream j, and its rows are final once
+    the calls at the order positions in ``after`` have completed (the latest
+    call on every stream so far, chunk i's own included).  Calls on one
+    stream complete in order, so every earlier call is covered."""
+    order = list(range(num_chunks))
+    if bwd_order == "descending":
+        order = order[::-1]
+    latest = [None] * bwd_streams
+    plan = []
+    for n, i in enumerate(order):
+        j = n % bwd_streams
+        latest[j] = n
+        plan.append((i, j, [x for x in latest if x is not None]))
+    return plan
+
+
 def backward_chunks(q, k, v, d_o, chunk, bufs, scale=None, stream=None, bwd_streams=None,
                     bwd_order="descending", on_final=None, before_chunk=None):
     """Backward every chunk of ``bufs`` (after ``forward_chunks``): dQ rows
@@ -384,13 +402,11 @@ def backward_chunks(q, k, v, d_o, chunk, bufs, scale=None, stream=None, bwd_stre
     sides = side_streams(q.device, bwd_streams - 1)
     for sd in sides:
         sd.wait_stream(main)
-    order = list(enumerate(bufs.starts))
-    if bwd_order == "descending":
-        order = order[::-1]
-    last = [None] * bwd_streams            # event after each stream's latest chunk
-    for n, (i, s) in enumerate(order):
+    need_events = on_final is not None or bwd_streams > 1
+    events = []                             # event after the call at each order position
+    for i, j, after in relay_plan(len(bufs.starts), bwd_streams, bwd_order):
+        s = bufs.starts[i]
         e = min(s + chunk, T)
-        j = n % bwd_streams
         st = main if j == 0 else sides[j - 1]
         if before_chunk is not None:
             before_chunk(i, st)
@@ -401,14 +417,12 @@ def backward_chunks(q, k, v, d_o, chunk, bufs, scale=None, stream=None, bwd_stre
                       tgt, bufs.dk, bufs.dv, s, s, scale, bufs.workspace_for(j), st)
             if tgt is not dq_c:
                 dq_c.copy_(tgt)
-        if on_final is not None or bwd_streams > 1:
+        if need_events:
             ev = torch.cuda.Event()
             ev.record(st)
-            last[j] = ev
+            events.append(ev)
         if on_final is not None:
-            # chunks i+1 .. i+bwd_streams-1 were each the latest on one of
-            # the other streams; every earlier chunk ran before one of them
-            on_final(i, s, e, [x for x in last if x is not None])
+            on_final(i, s, e, [events[m] for m in after])
     for sd in sides:
         main.wait_stream(sd)
 

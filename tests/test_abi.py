@@ -193,3 +193,26 @@ def test_backward_chunks_guards():
     with pytest.raises(ValueError, match="relay"):
         binding.backward_chunks(q16, q16, q16, q16, 128, None, bwd_streams=1, bwd_order="ascending",
                                 on_final=lambda *a: None)
+
+
+@pytest.mark.parametrize("D", [1, 2, 5, 16])
+@pytest.mark.parametrize("streams", [1, 2, 3, 4])
+def test_relay_plan_hands_on_only_final_rows(D, streams):
+    """SeCO's relay with overlapping backward calls: the rows of chunk i may
+    be handed on (weight gradients, host copy) only after every call that adds
+    into them -- chunks i..D-1, all issued before or at chunk i's -- has
+    completed.  Each such call must be covered by a waited call on its own
+    stream at the same or a later position (calls on a stream complete in
+    order)."""
+    plan = binding.relay_plan(D, streams)
+    stream_of = {}
+    for n, (i, j, after) in enumerate(plan):
+        assert i == D - 1 - n                  # last to first
+        assert j == n % streams                # round robin over the streams
+        stream_of[n] = j
+        assert n in after
+        assert len(after) == min(n + 1, streams)
+        for m in range(n + 1):
+            assert any(stream_of[w] == stream_of[m] and w >= m for w in after), (n, m)
+    asc = binding.relay_plan(D, streams, "ascending")
+    assert [i for i, _, _ in asc] == list(range(D))
