@@ -1,9 +1,12 @@
-"""ctypes binding of libseqattn (include/seqattn.h): argument marshalling only.
+"""ctypes binding of libseqattn (include/seqattn.h).
 
-Every step of the computation runs in the library's CUDA kernels; this module
-turns torch tensors into device pointers and sizes, passes the current torch
-CUDA stream, and raises ``SeqattnError`` on a non-OK status.  If the library
-has not been built, the first call raises; there is no other code path.
+Every step of the computation runs in the library's CUDA kernels.  The call
+wrappers turn torch tensors into device pointers and sizes, pass the torch
+CUDA stream, and raise ``SeqattnError`` on a non-OK status.  The layer drivers
+below them (``forward_chunks``, ``backward_chunks``, ``layer_forward_backward``,
+``LayerGraph``, ``HostLayerPass``) are host logic only: they order the chunk
+calls over CUDA streams and events, and do no arithmetic.  If the library has
+not been built, the first call raises; there is no other code path.
 """
 
 import ctypes
