@@ -229,29 +229,20 @@ def run_ours(args, w):
     main = torch.cuda.current_stream()
     n_fwd = binding.auto_fwd_streams(q, c)
     n_bwd = binding.auto_bwd_streams(q, k, c)
-    sides = binding.side_streams(dev, n_fwd - 1)
 
     def step(events=None):
+        # one layer pass: reset, chunk forwards 0..D-1 over n_fwd streams,
+        # chunk backwards D-1..0 over n_bwd streams; each pass is timed as a
+        # phase on the main stream, from its fork to its join
         binding.reset_accum(bufs.dk, bufs.dv, w.hq)
-        # chunk forwards spread over streams as in binding.forward_chunks; the
-        # forward is timed as a phase, from the fork to the join
         if events is not None:
-            events["fwd"][0].record(main)
-        for sd in sides:
-            sd.wait_stream(main)
-        for i, s in enumerate(starts):
-            e = min(s + c, T)
-            st = main if i % n_fwd == 0 else sides[i % n_fwd - 1]
-            binding.chunk_fwd(q[:, s:e], k, v, bufs.o[:, s:e], bufs.lse_chunks[i], s, stream=st)
-        for sd in sides:
-            main.wait_stream(sd)
+            events["start"].record(main)
+        binding.forward_chunks(q, k, v, c, bufs, None, main, n_fwd)
         if events is not None:
-            events["fwd"][1].record(main)
-        # chunk backwards D-1..0 over n_bwd streams (binding.backward_chunks),
-        # timed as a phase from the fork to the join
+            events["fwd_end"].record(main)
         binding.backward_chunks(q, k, v, do, c, bufs, None, main, n_bwd)
         if events is not None:
-            events["bwd"][1].record(main)
+            events["bwd_end"].record(main)
 
     if (T % c) != 0 or w.batch != 1:
         raise SystemExit("bench expects B=1 and T divisible by the chunk")
@@ -263,7 +254,7 @@ def run_ours(args, w):
     def ev():
         return torch.cuda.Event(enable_timing=True)
 
-    launch_ev = [{"fwd": (ev(), ev()), "bwd": (None, ev())} for _ in range(args.steps)]
+    launch_ev = [{"start": ev(), "fwd_end": ev(), "bwd_end": ev()} for _ in range(args.steps)]
     gpu_id = None
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -290,8 +281,8 @@ def run_ours(args, w):
 
     # roofline of both passes, each timed as a phase of every timed step (live
     # CUDA events on the main stream, from the fork to the join of its streams)
-    fwd_ms = sum(e["fwd"][0].elapsed_time(e["fwd"][1]) for e in launch_ev)
-    bwd_ms = sum(e["fwd"][1].elapsed_time(e["bwd"][1]) for e in launch_ev)
+    fwd_ms = sum(e["start"].elapsed_time(e["fwd_end"]) for e in launch_ev)
+    bwd_ms = sum(e["fwd_end"].elapsed_time(e["bwd_end"]) for e in launch_ev)
     pairs = sum(workloads.causal_pairs(s, min(c, T - s)) for s in starts)
     fwd_flops = 4 * w.batch * w.hq * w.head_dim * pairs * args.steps
     bwd_flops = 10 * w.batch * w.hq * w.head_dim * pairs * args.steps
