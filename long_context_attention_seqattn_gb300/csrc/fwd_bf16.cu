@@ -28,7 +28,9 @@
 // Only key tiles that reach past the tile's first query row carry the causal
 // mask (one or two tiles, since chunks may start anywhere).  The running
 // maxima are rescaled lazily: O_h and l_h are only corrected when a row max
-// grows by more than 2^8 (P stays below 256).
+// grows by more than 2^8 (P stays below 256).  Every wait sleeps in its
+// mbarrier (Watchdog::wait_sleep) rather than spinning, so waiting warps
+// leave their sub-partition's issue slots to the softmax warps.
 #include <cuda_bf16.h>
 
 #include "internal.h"
