@@ -77,3 +77,40 @@ def layer_inputs(w, device="cpu", seed=None):
     v = draw("v", seed, w.batch, w.seq, w.hkv, w.head_dim, dt, device)
     do = draw("do", seed, w.batch, w.seq, w.hq, w.head_dim, dt, device)
     return q, k, v, do
+
+
+def planted_growth_inputs(batch, seq, hq, hkv, head_dim, seed, dtype=torch.bfloat16, jump_log2=10.0,
+                          period=96, levels=3, width=16):
+    """Q, K, V, dO whose score row maxima rise along the key axis.
+
+    The iid N(0, 1) tensors of ``draw`` give scores of about N(0, 1) after the
+    1/sqrt(d) scale, so a row's maximum hardly moves once the first key tile
+    has been seen.  These inputs make it move.  Coordinates [0, width) of key
+    row j are overwritten with beta * min(floor(j / period), levels) /
+    sqrt(width) (a staircase that rises every ``period`` keys for ``levels``
+    steps, then stays flat), and the same coordinates of query row r of head
+    h with alpha / sqrt(width) when h % 4 == 0 or (r + h) % 3 != 0, and with 0
+    otherwise (every row of heads 0, 4, ...; two rows in three of the others).
+    The planted part of a score is then alpha * beta * stair; with the scale
+    1/sqrt(head_dim) each stair lifts the score of a planted row by
+    ``jump_log2`` in base-2 units (alpha beta = jump_log2 ln(2) sqrt(d)), so its
+    maximum grows by that much every ``period`` keys, while the unplanted rows
+    in between keep flat scores.  alpha = beta * levels (the geometric middle)
+    and the spread over ``width`` coordinates keep every planted entry small,
+    which keeps the bf16 rounding of P and dS from being magnified in dQ and
+    dK.  V and dO are the plain draws.  Everything else is as in ``draw``."""
+    q = draw("q", seed, batch, seq, hq, head_dim, torch.float32)
+    k = draw("k", seed, batch, seq, hkv, head_dim, torch.float32)
+    v = draw("v", seed, batch, seq, hkv, head_dim, dtype)
+    do = draw("do", seed, batch, seq, hq, head_dim, dtype)
+    prod = jump_log2 * 0.6931471805599453 * head_dim ** 0.5   # alpha * beta
+    alpha = (prod * levels) ** 0.5
+    beta = prod / alpha
+    spread = width ** -0.5
+    stairs = torch.clamp(torch.div(torch.arange(seq), period, rounding_mode="floor"), max=levels)
+    k[:, :, :, :width] = (beta * spread * stairs.to(torch.float32))[None, :, None, None]
+    rows = torch.arange(seq)[:, None]
+    heads = torch.arange(hq)[None, :]
+    planted = (heads % 4 == 0) | ((rows + heads) % 3 != 0)
+    q[:, :, :, :width] = torch.where(planted, alpha * spread, 0.0)[None, :, :, None]
+    return q.to(dtype), k.to(dtype), v, do

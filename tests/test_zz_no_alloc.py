@@ -5,8 +5,9 @@ The no-alloc entry point exists for callers that cannot allocate device
 memory: their memory belongs to another allocator and the interface they call
 through passes only the tensors, so they cannot hand the regular backward its
 workspace.  Its scratch is a fixed array inside the library that every call
-shares, so this test also calls it twice in a row and checks that the second
-call does not depend on what the first left behind.  The file name sorts last
+shares, so this test calls it twice in a row, each time right after a call
+for a longer chunk with other inputs has filled more of that array, and
+checks that the result does not depend on what was left behind.  The file name sorts last
 so that a run stopping at the first failure has already run every other test.
 """
 
@@ -20,16 +21,16 @@ from long_context_attention_seqattn_gb300 import binding, build, inputs
 
 pytestmark = pytest.mark.gpu
 
-BF16_REL = 2e-2
-BF16_ABS = 5e-2
+# Both backwards run the same kernels on the same inputs: they differ only in
+# the order of the fp32 atomic additions into dq, so the bar is tight.
+SAME_KERNELS_REL = 1e-5
 
 
 def _close(name, got, ref):
     got = got.double().cpu().numpy()
     ref = ref.double().cpu().numpy()
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
-    mx = np.abs(got - ref).max()
-    assert rel <= BF16_REL and mx <= BF16_ABS, f"{name}: rel-L2 {rel:.3e} max-abs {mx:.3e}"
+    assert rel <= SAME_KERNELS_REL, f"{name}: rel-L2 {rel:.3e}"
 
 
 def _p(t):
@@ -63,9 +64,24 @@ def test_noalloc_backward_matches_workspace_backward(dtype, q_start, c, d):
     binding.chunk_bwd(qc, k, v, o, lse, doc, dq_ref, dk_ref, dv_ref, q_start)
     binding.sync_status()
 
+    # a different, longer chunk (the whole sequence, other dO) whose row
+    # statistics fill more of the shared scratch than the checked call needs
+    o_f = torch.empty_like(q)
+    lse_f = torch.empty((B, Hq, T), dtype=torch.float32, device="cuda")
+    binding.chunk_fwd(q, k, v, o_f, lse_f, 0)
+    do_f = inputs.draw("do", 78, B, T, Hq, d, dt).cuda()
+    filler = [torch.empty(q.shape, dtype=torch.float32, device="cuda"),
+              torch.zeros(k.shape, dtype=torch.float32, device="cuda"),
+              torch.zeros(k.shape, dtype=torch.float32, device="cuda")]
+
     pb = binding.problem_for(k, Hq, dt)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for call in range(2):
+        # the scratch keeps what the previous call left; the checked call must
+        # rewrite every statistic it reads
+        st = lib.seqattn_chunk_bwd_noalloc(ctypes.byref(pb), 0, T, 0, d ** -0.5, _p(q), _p(k), _p(v),
+                                           _p(o_f), _p(lse_f), _p(do_f), *(_p(t) for t in filler), stream)
+        assert st == 0, lib.seqattn_last_error().decode()
         dq = torch.full(qc.shape, float("nan"), dtype=torch.float32, device="cuda")
         dk = torch.zeros(k.shape, dtype=torch.float32, device="cuda")
         dv = torch.zeros(k.shape, dtype=torch.float32, device="cuda")
