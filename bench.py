@@ -28,7 +28,8 @@ if ROOT not in sys.path:
 
 METRIC = "chunked causal attn fwd+bwd TFLOP/s (causal FLOPs) and % of GB300 BF16 peak"
 UNIT = "TFLOP/s"
-FALLBACK_SUSTAINED_TFLOPS = 1700.0   # used only when no measured peaks file exists
+FALLBACK_BURST_TFLOPS = 1900.0       # used only when no measured peaks file exists
+FALLBACK_SUSTAINED_TFLOPS = 1700.0
 
 # DRAM traffic (bytes read + written) per backward launch, from the ncu
 # launch list of a workload (average over its chunk launches), keyed by the
@@ -50,6 +51,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-wgrad", action="store_true")
+    ap.add_argument("--oracle-only", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--no-single-core", action="store_true",
+                    help="skip the one-core oracle timing of the cpu_baseline")
     ap.add_argument("--oracle-threads", type=int, default=None,
                     help="BLAS threads of the float64 oracle (cpu_baseline and --impl reference); "
                          "default: every core of the process's affinity mask")
@@ -107,14 +111,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def measured_peak():
+def measured_peaks():
+    """Dense bf16 peaks from the generated MEASURED_PEAKS.json: the burst
+    figure (a cuBLAS GEMM timed alone) is the roofline denominator for the
+    kernels of a step of a few tens of milliseconds; the sustained figure (the
+    same GEMM looped for seconds under the power cap) is reported beside it,
+    with the SM clock it was measured at."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as fh:
             pk = json.load(fh)
-        return float(pk["bf16_tflops_sustained"]), "measured (sustained cuBLAS bf16, MEASURED_PEAKS.json)"
+        clk = pk.get("clocks_under_load", {}).get("sm_mhz_median")
+        return {"burst": float(pk["bf16_tflops"]), "sustained": float(pk["bf16_tflops_sustained"]),
+                "sustained_sm_mhz": clk,
+                "source": "measured (cuBLAS bf16 GEMM, MEASURED_PEAKS.json)"}
     except (OSError, KeyError, ValueError):
-        return FALLBACK_SUSTAINED_TFLOPS, "fallback (sustained bf16)"
+        return {"burst": FALLBACK_BURST_TFLOPS, "sustained": FALLBACK_SUSTAINED_TFLOPS,
+                "sustained_sm_mhz": None, "source": "fallback (one earlier GB300 measurement)"}
 
 
 # ------------------------------------------------------------------ CPU oracle sample
@@ -155,14 +168,80 @@ def oracle_sample(w, seed, heads):
 ORACLE_THREADS = None   # set from --oracle-threads before NumPy is imported
 
 
+def affinity_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def host_cores():
     """Threads the oracle's BLAS may use: the affinity mask's cores, or fewer
     when --oracle-threads caps them."""
-    try:
-        n = len(os.sched_getaffinity(0))
-    except AttributeError:
-        n = os.cpu_count() or 1
+    n = affinity_cores()
     return min(n, ORACLE_THREADS) if ORACLE_THREADS else n
+
+
+def blas_info():
+    """Name and live thread count of the BLAS library NumPy loaded (OpenBLAS
+    reports its count through its own exported query function)."""
+    import ctypes
+
+    import numpy as np
+    a = np.ones((64, 64))
+    a @ a                                     # make sure the BLAS library is loaded
+    info = {"library": None, "threads": None}
+    try:
+        with open("/proc/self/maps") as fh:
+            libs = sorted({ln.split()[-1] for ln in fh if "blas" in ln.lower() and ln.split()[-1].startswith("/")})
+    except OSError:
+        libs = []
+    for path in libs:
+        info["library"] = os.path.basename(path)
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for sym in ("scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads",
+                    "openblas_get_num_threads64_", "openblas_get_num_threads"):
+            fn = getattr(lib, sym, None)
+            if fn is not None:
+                fn.restype = ctypes.c_int
+                info["threads"] = int(fn())
+                return info
+    return info
+
+
+def cpu_baseline_record(value, seconds, desc):
+    """cpu_baseline object of the bench line: the oracle's rate on this host
+    with the cores it could use and the BLAS threads it actually ran with."""
+    return {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle", "sample": desc,
+            "seconds": seconds, "affinity_cores": affinity_cores(), "cpu_count": os.cpu_count(),
+            "blas": blas_info()}
+
+
+def oracle_only(args, w):
+    """--oracle-only: time the oracle's bounded sample of workload ``w`` (all
+    query heads of key/value head 0) with the threads --oracle-threads allows
+    and print one JSON object; bench.py runs this in a child process for the
+    single-core baseline, since the BLAS thread pool is sized at import."""
+    G = w.hq // w.hkv
+    f, s, desc = oracle_sample(w, w.seed, G)
+    rec = cpu_baseline_record(f / s / 1e12, s, desc)
+    rec["workload"] = w.name
+    print(json.dumps(rec), flush=True)
+
+
+def single_core_baseline(workload="qwen3-4b-layer-t8192-c512"):
+    """The oracle on one core (one BLAS thread, one-core affinity) on the
+    8192-token layer's sample, in a child process; None if it fails."""
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-only", "--oracle-threads", "1",
+           "--workload", workload]
+    try:
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=300)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except (OSError, ValueError, IndexError, subprocess.TimeoutExpired):
+        return None
 
 
 # ------------------------------------------------------------------ reference arm
@@ -188,8 +267,7 @@ def run_reference(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": workload_config(w),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": cpu_baseline_record(value, secs / args.steps, desc),
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -286,12 +364,17 @@ def run_ours(args, w):
     pairs = sum(workloads.causal_pairs(s, min(c, T - s)) for s in starts)
     fwd_flops = 4 * w.batch * w.hq * w.head_dim * pairs * args.steps
     bwd_flops = 10 * w.batch * w.hq * w.head_dim * pairs * args.steps
-    peak, peak_src = measured_peak()
+    pk = measured_peaks()
+    peak = pk["burst"]
     bwd_tf = bwd_flops / (bwd_ms / 1e3) / 1e12
     fwd_tf = fwd_flops / (fwd_ms / 1e3) / 1e12
+    # the step lasts tens of milliseconds at the clocks sampled below, so the
+    # burst figure is the denominator; the sustained one is shown beside it
     roofline = {"kernel": "seqattn_chunk_bwd (row-statistics pre-pass + bwd_bf16_kernel)", "bound": "tensor",
                 "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s", "frac": bwd_tf / peak,
-                "peak_source": peak_src,
+                "peak_source": pk["source"] + ", burst",
+                "peak_sustained": pk["sustained"], "frac_sustained": bwd_tf / pk["sustained"],
+                "peak_sustained_sm_mhz": pk["sustained_sm_mhz"], "sm_mhz_timed": clock_info.get("sm_mhz"),
                 "traffic": BWD_TRAFFIC_BYTES_PER_LAUNCH.get(w.name),
                 "per_launch": f"causal bwd FLOPs 10*Hq*d*pairs(chunk) over the {D} chunk backwards of a "
                               f"step, timed as a phase ({n_bwd} stream(s), fork to join); avg_launch_ms is "
@@ -300,6 +383,7 @@ def run_ours(args, w):
                 "avg_launch_ms": bwd_ms / (D * args.steps)}
     roofline_fwd = {"kernel": "seqattn_chunk_fwd (fwd_bf16_kernel)", "bound": "tensor", "achieved": fwd_tf,
                     "peak": peak, "unit": "TFLOP/s", "frac": fwd_tf / peak,
+                    "frac_sustained": fwd_tf / pk["sustained"],
                     "per_phase": f"causal fwd FLOPs 4*Hq*d*pairs over the {D} chunk forwards of a step, "
                                  f"timed from the {n_fwd}-stream fork to the join",
                     "phase_ms": fwd_ms / args.steps}
@@ -342,14 +426,13 @@ def run_ours(args, w):
         h = inputs.draw("h", seed, w.batch, w.seq, 1, dm, torch.bfloat16, dev)[:, :, 0].contiguous()
         dws = [torch.zeros((dm, n), device=dev) for n in (w.hq * w.head_dim, w.hkv * w.head_dim,
                                                          w.hkv * w.head_dim)]
-        ws = torch.empty(binding.wgrad_workspace_size(w.batch, c, dm), dtype=torch.uint8, device=dev)
 
         def wgrad_pass():
             for i in range(D - 1, -1, -1):
                 s = starts[i]
                 e = min(s + c, T)
                 for g, dw in ((bufs.dq, dws[0]), (bufs.dk, dws[1]), (bufs.dv, dws[2])):
-                    binding.proj_wgrad(h, g, dw, s, e, ws)
+                    binding.proj_wgrad(h, g, dw, s, e)
 
         for _ in range(2):
             wgrad_pass()
@@ -365,16 +448,17 @@ def run_ours(args, w):
         wg_flops = 2.0 * w.batch * w.seq * dm * (w.hq + 2 * w.hkv) * w.head_dim
         wgrad = {"metric": "projection weight-gradient TFLOP/s (dW_q, dW_k, dW_v of one pass)",
                  "value": wg_flops / (wg_ms / 1e3) / 1e12, "unit": UNIT, "ms_per_pass": wg_ms,
-                 "d_model": dm, "kernels": "rows_to_bf16_kernel + cuBLASLt bf16 GEMM (float32 accumulate)",
-                 "launches_per_pass": 6 * D}
-        del h, dws, ws
+                 "d_model": dm, "kernels": "wgrad_bf16_kernel (tcgen05, g rounded to bf16 in the kernel, float32 accumulate)",
+                 "launches_per_pass": 3 * D}
+        del h, dws
 
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         G = w.hq // w.hkv
         f, s, desc = oracle_sample(w, w.seed, G)
-        cpu_baseline = {"value": f / s / 1e12, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-                        "sample": desc, "seconds": s}
+        cpu_baseline = cpu_baseline_record(f / s / 1e12, s, desc)
+        if not args.no_single_core:
+            cpu_baseline["single_core"] = single_core_baseline()
 
     launches_per_step = 1 + D + 2 * D   # reset, fwd per chunk, (statistics pre-pass + bwd) per chunk
     line = {
@@ -382,7 +466,7 @@ def run_ours(args, w):
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(w),
-        "frac_of_peak": value / world / peak,
+        "frac_of_peak": value / world / peak, "frac_of_sustained_peak": value / world / pk["sustained"],
         "roofline": roofline, "roofline_fwd": roofline_fwd,
         "cpu_baseline": cpu_baseline, "e2e": e2e, "wgrad": wgrad,
         "gpu_launches": launches_per_step * args.steps,
@@ -430,7 +514,7 @@ def run_sweep(args, w):
     for r in rows:
         r["time_vs_unchunked"] = r["ms_per_step"] / base["ms_per_step"]
     first = rows[0]
-    peak, _ = measured_peak()
+    peak = measured_peaks()["burst"]
     line = {"metric": METRIC, "value": first["value"], "unit": UNIT, "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": first["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -450,7 +534,11 @@ def main():
             os.environ[var] = str(args.oracle_threads)
     from long_context_attention_seqattn_gb300 import workloads
     w = workloads.WORKLOADS[args.workload or workloads.BENCH_WORKLOAD]
-    if args.impl == "reference":
+    if args.oracle_only:
+        if args.oracle_threads == 1 and hasattr(os, "sched_setaffinity"):
+            os.sched_setaffinity(0, {min(os.sched_getaffinity(0))})   # one core, before NumPy loads
+        oracle_only(args, w)
+    elif args.impl == "reference":
         run_reference(args, w)
     elif len(w.chunks) > 1:
         run_sweep(args, w)

@@ -181,22 +181,19 @@ seqattn_status seqattn_scale_accum_rows(const seqattn_problem* pb, int64_t row_b
  *   g: [batch, seq_len, n] float32 (dQ with n = Hq d, or dK / dV with
  *      n = Hkv d)
  *   dw: [d_model, n] float32, row-major, accumulated (never overwritten)
- * g is rounded to bf16 (nearest even) into the workspace, then a cuBLASLt
- * bf16 GEMM with float32 accumulation adds into dw, one GEMM per batch entry.
- * Requires batch >= 1, 0 <= row_begin <= row_end <= seq_len, d_model and n
- * positive multiples of 8, 16-byte aligned pointers, and a 256-byte aligned
- * workspace of at least seqattn_proj_wgrad_workspace_size(batch,
- * row_end - row_begin, n) bytes.  Async on `stream`; INVALID_ARG before any
- * launch on a bad argument, SEQATTN_ERR_CUDA if cuBLASLt fails.
+ * One tensor-core kernel: g is rounded to bf16 (nearest even) as it is read,
+ * the products are summed in float32 and added into dw with a plain
+ * load-add-store, so two calls that update the same dw must not run
+ * concurrently (calls on one stream are ordered).  Rows of h outside
+ * [row_begin, row_end) are read only where they meet a zero of g and must be
+ * finite.  Requires batch >= 1, 0 <= row_begin <= row_end <= seq_len,
+ * d_model and n positive multiples of 8, and 16-byte aligned pointers.  No
+ * workspace.  Async on `stream`; INVALID_ARG before any launch on a bad
+ * argument; row_begin == row_end is a no-op.
  */
 seqattn_status seqattn_proj_wgrad(int32_t batch, int64_t seq_len, int64_t row_begin,
                                   int64_t row_end, int32_t d_model, int32_t n, const void* h,
-                                  const float* g, float* dw, void* workspace,
-                                  size_t workspace_bytes, seqattn_stream_t stream);
-
-/* Bytes of workspace seqattn_proj_wgrad needs (0 for invalid sizes).  Pure
- * host function. */
-size_t seqattn_proj_wgrad_workspace_size(int32_t batch, int64_t rows, int32_t n);
+                                  const float* g, float* dw, seqattn_stream_t stream);
 
 /* Bytes of workspace seqattn_chunk_bwd needs for a chunk of q_len rows
  * (0 for an invalid problem).  Pure host function. */
@@ -206,6 +203,19 @@ size_t seqattn_bwd_workspace_size(const seqattn_problem* pb, int64_t q_len);
  * SEQATTN_ERR_TIMEOUT if a kernel gave up a bounded wait since the last
  * check, SEQATTN_ERR_CUDA if the synchronisation failed, else SEQATTN_OK. */
 seqattn_status seqattn_sync_status(seqattn_stream_t stream);
+
+/* Limit, in SM clock cycles, of every bounded device-side wait in the kernels
+ * launched after this call from any host thread of the process; cycles <= 0
+ * restores the default (2e9 cycles, about one second).  This is the knob that
+ * lets a caller (or a test) see the timeout path work without a GPU fault: a
+ * launch with a limit far below the microseconds its waits normally take has
+ * its waits run out, its CTAs let every copy and MMA already issued complete,
+ * release their tensor memory and return, and the next seqattn_sync_status()
+ * reports SEQATTN_ERR_TIMEOUT; outputs of such a launch are unspecified.
+ * Limits below 65536 cycles also make the forward's waits spin instead of
+ * sleeping in the barrier.  Pure host function (takes effect at the next
+ * launch). */
+void seqattn_set_wait_limit(int64_t cycles);
 
 /* Static description of a status code.  Pure host function. */
 const char* seqattn_status_string(seqattn_status s);

@@ -32,9 +32,9 @@ EXPORTED = (
     "seqattn_reset_accum",
     "seqattn_scale_accum_rows",
     "seqattn_proj_wgrad",
-    "seqattn_proj_wgrad_workspace_size",
     "seqattn_bwd_workspace_size",
     "seqattn_sync_status",
+    "seqattn_set_wait_limit",
     "seqattn_status_string",
     "seqattn_last_error",
 )
@@ -84,14 +84,14 @@ def load_library(path=LIB_PATH):
     lib.seqattn_scale_accum_rows.argtypes = [P, i64, i64, f32, vp, vp, vp]
     lib.seqattn_scale_accum_rows.restype = ctypes.c_int
     i32 = ctypes.c_int32
-    lib.seqattn_proj_wgrad.argtypes = [i32, i64, i64, i64, i32, i32, vp, vp, vp, vp, sz, vp]
+    lib.seqattn_proj_wgrad.argtypes = [i32, i64, i64, i64, i32, i32, vp, vp, vp, vp]
     lib.seqattn_proj_wgrad.restype = ctypes.c_int
-    lib.seqattn_proj_wgrad_workspace_size.argtypes = [i32, i64, i32]
-    lib.seqattn_proj_wgrad_workspace_size.restype = sz
     lib.seqattn_bwd_workspace_size.argtypes = [P, i64]
     lib.seqattn_bwd_workspace_size.restype = sz
     lib.seqattn_sync_status.argtypes = [vp]
     lib.seqattn_sync_status.restype = ctypes.c_int
+    lib.seqattn_set_wait_limit.argtypes = [i64]
+    lib.seqattn_set_wait_limit.restype = None
     lib.seqattn_status_string.argtypes = [ctypes.c_int]
     lib.seqattn_status_string.restype = ctypes.c_char_p
     lib.seqattn_last_error.argtypes = []
@@ -176,12 +176,17 @@ def chunk_bwd(q, k, v, o, lse, d_o, dq, dk_accum, dv_accum, q_start, prefix_len=
     pb = problem_for(k, Hq, q.dtype)
     lib = load_library()
     need = int(lib.seqattn_bwd_workspace_size(ctypes.byref(pb), c))
-    if workspace is None:
+    temp = workspace is None
+    if temp:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     _check(lib.seqattn_chunk_bwd(ctypes.byref(pb), q_start, c, prefix_len, scale, _ptr(q), _ptr(k),
                                  _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk_accum),
                                  _ptr(dv_accum), _ptr(workspace), workspace.numel(),
                                  _stream(stream)))
+    if temp and stream is not None:
+        # the temporary was allocated on the current stream but is read on
+        # `stream`: keep the caching allocator from reusing it before then
+        workspace.record_stream(stream)
 
 
 def reset_accum(dk_accum, dv_accum, num_q_heads=None, stream=None):
@@ -206,12 +211,7 @@ def scale_accum_rows(dk_accum, dv_accum, row_begin, row_end, scale, stream=None)
                                                    _ptr(dk_accum), _ptr(dv_accum), _stream(stream)))
 
 
-def wgrad_workspace_size(batch, rows, n):
-    """Bytes of workspace ``proj_wgrad`` needs for ``rows`` rows of width ``n``."""
-    return int(load_library().seqattn_proj_wgrad_workspace_size(batch, rows, n))
-
-
-def proj_wgrad(h, g, dw, row_begin, row_end, workspace=None, stream=None):
+def proj_wgrad(h, g, dw, row_begin, row_end, stream=None):
     """dw [d_model, n] += sum over batch entries of h[b, r0:r1]^T g[b, r0:r1],
     with h [B, T, d_model] bf16 (hidden states) and g [B, T, ...] float32 (dQ,
     dK or dV; trailing dims flattened to n)."""
@@ -222,16 +222,19 @@ def proj_wgrad(h, g, dw, row_begin, row_end, workspace=None, stream=None):
     _need(dw, "dw", torch.float32, (dm, n))
     if tuple(g.shape[:2]) != (B, T):
         raise ValueError(f"g has leading shape {tuple(g.shape[:2])}, expected {(B, T)}")
-    need = wgrad_workspace_size(B, row_end - row_begin, n)
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=h.device)
     _check(load_library().seqattn_proj_wgrad(B, T, row_begin, row_end, dm, n, _ptr(h), _ptr(g), _ptr(dw),
-                                             _ptr(workspace), workspace.numel(), _stream(stream)))
+                                             _stream(stream)))
 
 
 def sync_status(stream=None):
     """Synchronise the stream and raise if a kernel gave up a bounded wait."""
     _check(load_library().seqattn_sync_status(_stream(stream)))
+
+
+def set_wait_limit(cycles):
+    """Limit (SM cycles) of the kernels' bounded waits for later launches;
+    ``cycles <= 0`` restores the default of about one second."""
+    load_library().seqattn_set_wait_limit(int(cycles))
 
 
 def status_string(code):
@@ -459,7 +462,6 @@ def layer_forward_backward(q, k, v, d_o, chunk, scale=None, bufs=None, stream=No
     on_final = None
     relay = main
     if wgrad is not None:
-        ws = torch.empty(wgrad_workspace_size(B, chunk, Hq * d), dtype=torch.uint8, device=q.device)
         if bwd_streams > 1:
             relay = side_streams(q.device, bwd_streams)[bwd_streams - 1]
             relay.wait_stream(main)
@@ -470,7 +472,7 @@ def layer_forward_backward(q, k, v, d_o, chunk, scale=None, bufs=None, stream=No
                 for ev in events:
                     relay.wait_event(ev)
             for g, dw in ((bufs.dq, dw_q), (bufs.dk, dw_k), (bufs.dv, dw_v)):
-                proj_wgrad(h, g, dw, s, e, ws, relay)
+                proj_wgrad(h, g, dw, s, e, relay)
 
     backward_chunks(q, k, v, d_o, chunk, bufs, scale, main, bwd_streams, bwd_order, on_final)
     if relay is not main:

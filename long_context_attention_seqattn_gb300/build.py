@@ -17,8 +17,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libseqattn.so")
 
-SOURCES = ["seqattn_api.cu", "simt_f32.cu", "fwd_bf16.cu", "bwd_bf16.cu", "wgrad.cu"]
-LIBS = ["-lcublasLt"]
+SOURCES = ["seqattn_api.cu", "simt_f32.cu", "fwd_bf16.cu", "bwd_bf16.cu", "wgrad_bf16.cu"]
+LIBS = []
 HEADERS = ["internal.h", "sm103_ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

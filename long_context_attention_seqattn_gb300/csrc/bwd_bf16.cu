@@ -106,6 +106,7 @@ struct BwdParams {
   float* dk;
   float* dv;
   unsigned int* err;
+  long long wait_cycles;
 };
 
 struct BwdBarriers {
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ BwdBarriers bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
-  Watchdog wd{&abort_flag, p.err};
+  Watchdog wd(&abort_flag, p.err, p.wait_cycles);
 
   // ---- work item: (batch b, kv head g, key tile kt).
   // Per batch entry: first the key tiles that lie wholly before the chunk
@@ -250,6 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   auto step_head = [&](int n) { return g * p.G + n / nq; };
   auto step_qtile = [&](int n) { return qi_first + n % nq; };
+  int n_issued = 0;  // producer: steps issued into the ring so far
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -265,7 +267,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(smem + C::kOffK + blk * kKVHalf, &map_k, &bars.kv_full, 64 * blk, g, krow);
         tma_load_3d(smem + C::kOffV + blk * kKVHalf, &map_v, &bars.kv_full, 64 * blk, g, krow);
       }
-      int issued[kQStages] = {};
       for (int n = 0; n < n_steps; ++n) {
         const int st = n % kQStages;
         const uint32_t ph = (n / kQStages) & 1;
@@ -283,12 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       h, qrow);
         }
         bulk_load(stat + st * 2 * kBQ, p.stats + sblk, kStatBytes, &bars.q_full[st]);
-        issued[st] = n + 1;
-      }
-      if (wd.aborted()) {
-        wd.drain(&bars.kv_full, 0, 1000000);
-        for (int st = 0; st < kQStages; ++st)
-          if (issued[st] > 0) wd.drain(&bars.q_full[st], ((issued[st] - 1) / kQStages) & 1, 1000000);
+        n_issued = n + 1;
       }
     }
   } else if (warp == 1 || warp == kIssuerKV || warp == kIssuerDP) {
@@ -528,6 +524,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  if (wd.aborted()) {
+    // A wait ran out.  Every role has left its loop (the MMA issuers after
+    // their last MMA completed), but a copy issued before the abort may still
+    // be in flight: let it land before the CTA's shared memory goes away.
+    if (warp == 0 && lane == 0) {
+      wd.drain(&bars.kv_full, 0, 1000000);
+      for (int st = 0; st < kQStages && st < n_issued; ++st) {
+        const int last = st + kQStages * ((n_issued - 1 - st) / kQStages);  // last step issued into stage st
+        wd.drain(&bars.q_full[st], (last / kQStages) & 1, 1000000);
+      }
+    }
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
@@ -566,6 +575,7 @@ cudaError_t launch_bwd_bf16(const ChunkGeom& g, const Bf16BwdMaps& maps, const f
   p.dk = dk;
   p.dv = dv;
   p.err = err;
+  p.wait_cycles = g.wait_cycles;
   const unsigned grid = static_cast<unsigned>(p.n_ktiles) * g.Hkv * g.B;
   return g.d == 64 ? launch_bwd_bf16_d<64>(p, maps, grid, s) : launch_bwd_bf16_d<128>(p, maps, grid, s);
 }

@@ -81,6 +81,7 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   unsigned int* err;
+  long long wait_cycles;
 };
 
 struct FwdBarriers {
@@ -127,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ FwdBarriers bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
-  Watchdog wd{&abort_flag, p.err};
+  Watchdog wd(&abort_flag, p.err, p.wait_cycles);
 
   // ---- work item: (b, kv group, head in group, q tile), q tile fastest and
   // heaviest (longest key range) first.
@@ -175,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_u32(smem + C::kOffQ);
   const uint32_t sK = smem_u32(smem + C::kOffK);
   const uint32_t sV = smem_u32(smem + C::kOffV);
+  int n_issued = 0;  // producers: tiles issued into their ring so far
 
   if (warp == 0 || warp == kVWarp) {
     // ------------------------------------------------------------ producers
@@ -195,7 +197,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int blk = 0; blk < D / 64; ++blk)
           tma_load_3d(smem + C::kOffQ + blk * kBlockBytes, &map_q, &bars.q_full, 64 * blk, h, qrow);
       }
-      int issued[kStages] = {};
       for (int t = 0; t < n_kv; ++t) {
         const int st = t % kStages;
         const uint32_t ph = (t / kStages) & 1;
@@ -205,13 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int blk = 0; blk < D / 64; ++blk)
           tma_load_3d(smem + off + st * kTileBytes + blk * kBlockBytes, map, &full[st], 64 * blk, g, krow);
-        issued[st] = t + 1;
-      }
-      if (wd.aborted()) {
-        // let copies already in flight land before the CTA's smem goes away
-        if (is_k) wd.drain(&bars.q_full, 0, 1000000);
-        for (int st = 0; st < kStages; ++st)
-          if (issued[st] > 0) wd.drain(&full[st], ((issued[st] - 1) / kStages) & 1, 1000000);
+        n_issued = t + 1;
       }
     }
   } else if (warp == 1 || warp == kPVWarp) {
@@ -411,6 +406,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  if (wd.aborted()) {
+    // A wait ran out.  Every role has left its loop (the MMA issuers after
+    // their last MMA completed), but a copy issued before the abort may still
+    // be in flight: let it land before the CTA's shared memory goes away.
+    if ((warp == 0 || warp == kVWarp) && lane == 0) {
+      uint64_t* full = warp == 0 ? bars.k_full : bars.v_full;
+      if (warp == 0) wd.drain(&bars.q_full, 0, 1000000);
+      for (int st = 0; st < kStages && st < n_issued; ++st) {
+        const int last = st + kStages * ((n_issued - 1 - st) / kStages);  // last tile issued into stage st
+        wd.drain(&full[st], (last / kStages) & 1, 1000000);
+      }
+    }
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
@@ -444,6 +453,7 @@ cudaError_t launch_fwd_bf16(const ChunkGeom& g, const Bf16FwdMaps& maps, void* o
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.err = err;
+  p.wait_cycles = g.wait_cycles;
   const unsigned grid = static_cast<unsigned>(p.n_qtiles) * g.Hq * g.B;
   return g.d == 64 ? launch_fwd_bf16_d<64>(p, maps, grid, s) : launch_fwd_bf16_d<128>(p, maps, grid, s);
 }

@@ -16,6 +16,7 @@ struct ChunkGeom {
   int64_t q_len;     // rows in the chunk
   int64_t kv_begin;  // first visible key row (q_start - prefix_len)
   float scale;       // softmax scale
+  long long wait_cycles;  // limit of every bounded device wait (SM cycles)
 };
 
 // ---- float32 exact path (SIMT FMA) ----------------------------------------
@@ -54,17 +55,11 @@ cudaError_t launch_fwd_bf16(const ChunkGeom& g, const Bf16FwdMaps& maps, void* o
 cudaError_t launch_bwd_bf16(const ChunkGeom& g, const Bf16BwdMaps& maps, const float* stats,
                             float* dq, float* dk, float* dv, unsigned int* err, cudaStream_t s);
 
-// ---- projection weight gradient (cuBLASLt bf16 GEMM) ----------------------
-// cuBLASLt's own scratch, carved from the caller's workspace after the bf16
-// copy of G.
-constexpr size_t kWgradLtWorkspace = size_t(32) << 20;
-struct WgradStatus {
-  cudaError_t cuda = cudaSuccess;
-  int blas = 0;  // cublasStatus_t
-};
-size_t wgrad_workspace_bytes(int32_t batch, int64_t rows, int32_t n);
-WgradStatus launch_wgrad(int32_t batch, int64_t seq_len, int64_t row_begin, int64_t row_end, int32_t d_model,
-                         int32_t n, const void* h, const float* g, float* dw, void* workspace,
-                         size_t workspace_bytes, cudaStream_t s);
+// ---- projection weight gradient (tcgen05, G rounded to bf16 in the kernel) -
+// map_h: 3-D bf16 tensor map over h [batch, seq_len, d_model] with a box of
+// {64 columns, 64 rows, 1 batch entry} and 128-byte swizzle.
+cudaError_t launch_wgrad_bf16(const CUtensorMap& map_h, int32_t batch, int64_t seq_len, int64_t row_begin,
+                              int64_t row_end, int32_t d_model, int32_t n, const float* g, float* dw,
+                              unsigned int* err, long long wait_cycles, cudaStream_t s);
 
 }  // namespace seqattn

@@ -1,13 +1,14 @@
 // seqattn_api.cu -- the C ABI declared in include/seqattn.h: argument
 // validation (before any launch), TMA tensor maps, the per-device error word,
 // and dispatch to the float32 and bf16 kernel families, the accumulator row
-// scaling and the projection weight gradient.
+// scaling and the projection weight gradient kernel.
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -46,6 +47,11 @@ seqattn_status cuda_fail(cudaError_t e, const char* where) {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 unsigned int* g_err_ptr[kMaxDevices] = {};
+
+// Limit of every bounded device wait of the kernels launched from now on
+// (seqattn_set_wait_limit); the default is about one second.
+constexpr long long kDefaultWaitCycles = 2000000000LL;
+std::atomic<long long> g_wait_cycles{kDefaultWaitCycles};
 
 // Device address of this device's error word (looked up once per device).
 cudaError_t error_word(unsigned int** out) {
@@ -96,6 +102,23 @@ bool make_map(CUtensorMap* m, const void* base, int d, int heads, int64_t rows, 
   return r == CUDA_SUCCESS;
 }
 
+// 3-D bf16 tensor map over a row-major [B, T, cols] tensor: box of {64
+// columns, box_rows rows, 1 batch entry}, 128-byte swizzle.  Rows past T and
+// columns past `cols` read as zero.
+bool make_map_btc(CUtensorMap* m, const void* base, int64_t B, int64_t T, int64_t cols, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  memset(m, 0, sizeof(*m));
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, static_cast<cuuint64_t>(T) * static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 seqattn_status check_problem(const seqattn_problem* pb) {
@@ -139,6 +162,7 @@ seqattn_status check_chunk(const seqattn_problem* pb, int64_t q_start, int64_t q
   g->q_len = q_len;
   g->kv_begin = q_start - prefix_len;
   g->scale = scale;
+  g->wait_cycles = g_wait_cycles.load(std::memory_order_relaxed);
   return SEQATTN_OK;
 }
 
@@ -265,35 +289,29 @@ seqattn_status seqattn_scale_accum_rows(const seqattn_problem* pb, int64_t row_b
   return e == cudaSuccess ? ok() : cuda_fail(e, "scale launch");
 }
 
-size_t seqattn_proj_wgrad_workspace_size(int32_t batch, int64_t rows, int32_t n) {
-  if (batch < 1 || rows < 0 || n < 8 || n % 8) return 0;
-  return wgrad_workspace_bytes(batch, rows, n);
-}
-
 seqattn_status seqattn_proj_wgrad(int32_t batch, int64_t seq_len, int64_t row_begin,
                                   int64_t row_end, int32_t d_model, int32_t n, const void* h,
-                                  const float* g, float* dw, void* workspace,
-                                  size_t workspace_bytes, seqattn_stream_t stream) {
+                                  const float* g, float* dw, seqattn_stream_t stream) {
   if (batch < 1 || seq_len < 1) return fail(SEQATTN_ERR_INVALID_ARG, "batch and seq_len must be >= 1");
   if (row_begin < 0 || row_end < row_begin || row_end > seq_len)
     return fail(SEQATTN_ERR_INVALID_ARG, "need 0 <= row_begin <= row_end <= seq_len (got %lld, %lld)",
                 (long long)row_begin, (long long)row_end);
   if (d_model < 8 || d_model % 8 || n < 8 || n % 8)
     return fail(SEQATTN_ERR_INVALID_ARG, "d_model (%d) and n (%d) must be positive multiples of 8", d_model, n);
-  if (static_cast<int64_t>(batch) * seq_len > INT32_MAX)
-    return fail(SEQATTN_ERR_INVALID_ARG, "batch * seq_len exceeds 2^31 - 1 rows");
-  seqattn_status s = check_ptrs({{h, "h"}, {g, "g"}, {dw, "dw"}, {workspace, "workspace"}});
+  if (static_cast<int64_t>(batch) * seq_len > INT32_MAX || seq_len * static_cast<int64_t>(n) > INT32_MAX)
+    return fail(SEQATTN_ERR_INVALID_ARG, "batch * seq_len or seq_len * n exceeds 2^31 - 1");
+  seqattn_status s = check_ptrs({{h, "h"}, {g, "g"}, {dw, "dw"}});
   if (s != SEQATTN_OK) return s;
-  const int64_t rows = row_end - row_begin;
-  if (workspace_bytes < wgrad_workspace_bytes(batch, rows, n))
-    return fail(SEQATTN_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes,
-                wgrad_workspace_bytes(batch, rows, n));
-  if (rows == 0) return ok();
-  WgradStatus w = launch_wgrad(batch, seq_len, row_begin, row_end, d_model, n, h, g, dw, workspace, workspace_bytes,
-                               reinterpret_cast<cudaStream_t>(stream));
-  if (w.cuda != cudaSuccess) return cuda_fail(w.cuda, "wgrad conversion launch");
-  if (w.blas != 0) return fail(SEQATTN_ERR_CUDA, "cuBLASLt returned status %d", w.blas);
-  return ok();
+  if (row_end == row_begin) return ok();
+  unsigned int* err = nullptr;
+  cudaError_t e = error_word(&err);
+  if (e != cudaSuccess) return cuda_fail(e, "error word");
+  CUtensorMap map_h;
+  if (!make_map_btc(&map_h, h, batch, seq_len, d_model, 64))
+    return fail(SEQATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for h");
+  e = launch_wgrad_bf16(map_h, batch, seq_len, row_begin, row_end, d_model, n, g, dw, err,
+                        g_wait_cycles.load(std::memory_order_relaxed), reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "wgrad launch");
 }
 
 size_t seqattn_bwd_workspace_size(const seqattn_problem* pb, int64_t q_len) {
@@ -316,6 +334,10 @@ seqattn_status seqattn_sync_status(seqattn_stream_t stream) {
     return fail(SEQATTN_ERR_TIMEOUT, "a kernel gave up a bounded wait (error word 0x%x)", w);
   }
   return ok();
+}
+
+void seqattn_set_wait_limit(int64_t cycles) {
+  g_wait_cycles.store(cycles > 0 ? cycles : kDefaultWaitCycles, std::memory_order_relaxed);
 }
 
 const char* seqattn_status_string(seqattn_status s) {

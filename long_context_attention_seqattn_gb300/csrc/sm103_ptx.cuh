@@ -23,9 +23,13 @@ enum : unsigned int {
   kErrMisaligned = 2u,  // shared-memory base not aligned as the kernel requires
 };
 
-// A wait gives up after this many SM clock cycles (~1 s at 2 GHz).  Every
-// legitimate wait in these kernels is microseconds long.
+// A wait gives up after this many SM clock cycles (~1 s at 2 GHz) unless the
+// launch carries another limit (seqattn_set_wait_limit).  Every legitimate
+// wait in these kernels is microseconds long.
 constexpr long long kWaitCycles = 2000000000LL;
+// Below this limit a wait checks the clock on every poll and never sleeps, so
+// a short limit runs out as soon as a phase is not already complete.
+constexpr long long kShortWaitCycles = 65536LL;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -90,6 +94,10 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 struct Watchdog {
   volatile int* abort_flag;  // in shared memory
   unsigned int* err;         // device error word
+  long long limit;           // SM cycles a wait may last
+
+  __device__ __forceinline__ Watchdog(volatile int* flag, unsigned int* e, long long cycles)
+      : abort_flag(flag), err(e), limit(cycles) {}
 
   __device__ __forceinline__ bool aborted() const { return *abort_flag != 0; }
 
@@ -100,16 +108,18 @@ struct Watchdog {
 
   // Wait until the phase with the given parity of `bar` has completed.
   // Returns false (and trips the watchdog) if the wait runs out or another
-  // thread of the CTA already gave up.
+  // thread of the CTA already gave up.  The clock is read every 64 polls, or
+  // on every poll under a short limit.
   __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
+    const uint32_t mask = limit < kShortWaitCycles ? 0u : 63u;
     uint32_t spins = 0;
     while (true) {
       if (mbar_try_wait(bar, parity)) return true;
-      if ((++spins & 63u) == 0) {
+      if ((++spins & mask) == 0) {
         if (aborted()) return false;
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > limit) {
           trip();
           return false;
         }
@@ -121,14 +131,15 @@ struct Watchdog {
   // suspend-time hint; the phase's completion wakes it) rather than spinning.
   // The forward kernel waits this way: measured on the 32768-token layer,
   // 1242-1245 against 1231-1233 TFLOP/s per forward launch.  The backward
-  // keeps spinning waits: sleeping cost it 3%.
+  // keeps spinning waits: sleeping cost it 3%.  Under a short limit it spins.
   __device__ __forceinline__ bool wait_sleep(uint64_t* bar, uint32_t parity) {
+    if (limit < kShortWaitCycles) return wait(bar, parity);
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     const long long t0 = clock64();
     while (true) {
       if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
       if (aborted()) return false;
-      if (clock64() - t0 > kWaitCycles) {
+      if (clock64() - t0 > limit) {
         trip();
         return false;
       }

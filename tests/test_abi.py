@@ -114,33 +114,22 @@ def test_scale_rows_validation(lib):
 def test_proj_wgrad_validation(lib):
     """Argument checks of seqattn_proj_wgrad, all refused before any launch."""
     f = lib.seqattn_proj_wgrad
-    big = 1 << 30
     ok_args = dict(batch=1, seq=64, r0=0, r1=32, dm=64, n=128)
 
     def call(**kw):
         a = dict(ok_args, **kw)
-        ptrs = kw.get("ptrs", [P, P, P, P])
-        return f(a["batch"], a["seq"], a["r0"], a["r1"], a["dm"], a["n"], *ptrs, kw.get("ws", big), NUL)
+        ptrs = kw.get("ptrs", [P, P, P])
+        return f(a["batch"], a["seq"], a["r0"], a["r1"], a["dm"], a["n"], *ptrs, NUL)
 
     assert call(batch=0) == 1
     assert call(r1=65) == 1                         # past seq_len
     assert call(r0=10, r1=9) == 1
     assert call(dm=60) == 1                         # not a multiple of 8
     assert call(n=4) == 1
-    assert call(ptrs=[P, NUL, P, P]) == 1
-    assert call(ptrs=[P, P, MIS, P]) == 1
-    assert call(ws=1024) == 1                       # workspace too small
-    assert b"workspace" in lib.seqattn_last_error()
-
-
-def test_proj_wgrad_workspace_size(lib):
-    lib.seqattn_proj_wgrad_workspace_size.restype = ctypes.c_size_t
-    lib.seqattn_proj_wgrad_workspace_size.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int32]
-    lt = 32 << 20                                   # cuBLASLt scratch
-    assert lib.seqattn_proj_wgrad_workspace_size(1, 2048, 4096) == 2048 * 4096 * 2 + lt
-    assert lib.seqattn_proj_wgrad_workspace_size(2, 3, 8) == 256 + lt       # rounded up to 256 bytes
-    assert lib.seqattn_proj_wgrad_workspace_size(0, 3, 8) == 0
-    assert lib.seqattn_proj_wgrad_workspace_size(1, 3, 12) == 0
+    assert call(ptrs=[P, NUL, P]) == 1
+    assert call(ptrs=[P, P, MIS]) == 1
+    assert b"aligned" in lib.seqattn_last_error()
+    assert call(r0=5, r1=5) == 0                    # empty row range: a no-op, nothing launched
 
 
 def test_empty_chunk_is_ok_without_touching_memory(lib):

@@ -302,10 +302,14 @@ def assert_wgrad(name, got, ref):
     assert r <= BF16_REL and a <= 1e-2 * float(np.abs(ref).max()), f"{name}: rel-L2 {r:.3e} max-abs {a:.3e}"
 
 
-def test_proj_wgrad_accumulates_h_transpose_g():
-    """dw += h^T g over a row range of every batch entry, twice (accumulation),
-    against the float64 oracle."""
-    B, T, dm, n, r0, r1 = 2, 300, 96, 136, 37, 261
+@pytest.mark.parametrize("B,T,dm,n,r0,r1", [
+    (2, 300, 96, 136, 37, 261),        # partial tiles everywhere: 224 rows, 96 of 256 d_model, 136 of 2 x 128 n
+    (1, 4096, 4096, 1024, 2048, 4096),  # a dK/dV-shaped chunk of the 32768-token layer's projections
+    (1, 1024, 640, 392, 0, 1000),      # 2.5 d_model tiles, 3 + 1/16 n tiles, ragged last stage
+])
+def test_proj_wgrad_accumulates_h_transpose_g(B, T, dm, n, r0, r1):
+    """dw += h^T g over a row range of every batch entry, twice (accumulation
+    onto a non-zero dw), against the float64 oracle."""
     h = inputs.draw("h", 5, B, T, 1, dm, torch.bfloat16)[:, :, 0]
     g = inputs.draw("do", 5, B, T, 1, n, torch.float32)[:, :, 0]
     dw = torch.zeros((dm, n), device="cuda")
@@ -414,19 +418,32 @@ def _sum_invariant(w, bufs):
     """sum_j dV[j] = sum over the group's rows of dO (softmax rows sum to one),
     at any size.  The sums run over T*G terms of magnitude ~1, so the
     element-wise absolute bar of the outputs does not apply to them: the check
-    is rel-L2 <= 2e-2 and max-abs <= 1e-3 of the largest |sum|."""
+    is rel-L2 <= 2e-2 and max-abs <= 1e-3 of the largest |sum|.  dO is
+    regenerated block by block, so the reference never holds the whole
+    tensor in float64."""
     G = w.hq // w.hkv
-    do = inputs.draw("do", w.seed, w.batch, w.seq, w.hq, w.head_dim, inputs.torch_dtype(w.dtype))
-    ref = do.to(torch.float64).view(w.batch, w.seq, w.hkv, G, w.head_dim).sum((1, 3)).numpy()
+    dt = inputs.torch_dtype(w.dtype)
+    ref = np.zeros((w.batch, w.hkv, w.head_dim))
+    for b in range(w.batch):
+        for r0 in range(0, w.seq, inputs.BLOCK_ROWS):
+            r1 = min(w.seq, r0 + inputs.BLOCK_ROWS)
+            blk = inputs.draw_rows("do", w.seed, b, r0, r1, w.hq, w.head_dim, dt).to(torch.float64)
+            ref[b] += blk.view(r1 - r0, w.hkv, G, w.head_dim).sum((0, 2)).numpy()
     got = bufs.dv.to(torch.float64).sum(1).cpu().numpy()
     r, a = rel_l2(got, ref), max_abs(got, ref)
     assert r <= BF16_REL and a <= 1e-3 * np.abs(ref).max(), f"sum_j dV: rel-L2 {r:.3e} max-abs {a:.3e}"
 
 
-def test_bf16_llama3_8b_layer_sampled():
+def test_bf16_llama3_8b_layer_full_groups():
+    """The 32768-token layer in the bench's launch configuration: every O,
+    LSE, dQ, dK and dV element of key/value groups 0 and 7 (their four query
+    heads each) against the oracle run on just those heads (groups are
+    independent), plus sampled rows and the dV column-sum invariant."""
     w = workloads.WORKLOADS["llama3-8b-layer-t32768-c2048"]
-    dev = inputs.layer_inputs(w, device="cuda")
-    bufs = run_layer(*dev, w.chunk)
+    cpu = inputs.layer_inputs(w)
+    bufs = run_layer(*[x.cuda() for x in cpu], w.chunk)
+    _bf16_group_check(w, cpu, bufs, w.chunk, (0, w.hkv - 1))
+    del cpu
     _sampled_check(w, bufs, (0, w.hkv - 1), sample_rows=(0, 1, 2047, 2048, 16383, 30720, 32767))
     _sum_invariant(w, bufs)
 
@@ -436,6 +453,7 @@ def test_bf16_32b_layer_t131072_sampled():
     dev = inputs.layer_inputs(w, device="cuda")
     bufs = run_layer(*dev, w.chunk)
     _sampled_check(w, bufs, (0,), sample_rows=(0, 4095, 4096, 65536, 131071))
+    _sum_invariant(w, bufs)
 
 
 def test_bf16_partition_sweep_agrees_with_unchunked():
