@@ -16,13 +16,14 @@
 // row segment per warp and row), round it to bf16 pairs and store them into a
 // ring of A slots in TMEM; no converted copy of G ever exists in HBM or
 // shared memory.  H comes in by TMA.
-//   warp 0      TMA producer of H (64 rows x 256 columns per stage, 4 stages)
+//   warp 0      TMA producer of H (64 rows x 256 columns per stage, 6 stages)
 //   warp 1      TMEM owner + MMA issuer (4 MMAs M128 N256 K16 per stage)
 //   warps 2..9  converters, one per TMEM lane quadrant and stage parity; then
 //               the epilogue: dW tile += D (load, add, store: within one call
 //               this CTA is the only writer of the tile)
 // TMEM (512 columns): the accumulator D in [0, 256), four A slots of 32
-// columns (64 rows as bf16 pairs) in [256, 384).
+// columns (64 rows as bf16 pairs) in [256, 384).  Each converter warp keeps
+// the loads of its next stage in flight while it converts the current one.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -34,7 +35,8 @@ namespace {
 constexpr int kBM = 128;               // dW columns (n) per CTA: the MMA's M
 constexpr int kBN = 256;               // dW rows (d_model) per CTA: the MMA's N
 constexpr int kBK = 64;                // rows (tokens) per stage
-constexpr int kStages = 4;
+constexpr int kStages = 6;             // shared-memory ring of H
+constexpr int kASlots = 4;             // TMEM ring of converted G
 constexpr int kConvWarps = 8;          // two per TMEM lane quadrant
 constexpr int kThreads = 32 * (2 + kConvWarps);
 constexpr int kBoxBytes = kBK * 128;   // one 64-column block of a stage: 64 rows x 128 B
@@ -59,7 +61,7 @@ struct WgradParams {
 
 struct WgradBarriers {
   uint64_t h_full[kStages], h_empty[kStages];
-  uint64_t a_full[kStages], a_empty[kStages];
+  uint64_t a_full[kASlots], a_empty[kASlots];
   uint64_t acc_full;
   uint64_t mma_final;
 };
@@ -98,7 +100,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bars.h_full[i], 1);
       mbar_init(&bars.h_empty[i], 1);
-      mbar_init(&bars.a_full[i], 4 * 32);    // the four converter warps of the stage's parity
+    }
+    for (int i = 0; i < kASlots; ++i) {
+      mbar_init(&bars.a_full[i], 4 * 32);    // the four converter warps of the slot's parity
       mbar_init(&bars.a_empty[i], 1);
     }
     mbar_init(&bars.acc_full, 1);
@@ -138,17 +142,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int s = 0; ok && s < n_st; ++s) {
         const int st = s % kStages;
-        const uint32_t ph = (s / kStages) & 1;
-        if (!(ok = wd.wait(&bars.h_full[st], ph))) break;
-        if (!(ok = wd.wait(&bars.a_full[st], ph))) break;
+        const int sl = s % kASlots;
+        if (!(ok = wd.wait(&bars.h_full[st], (s / kStages) & 1))) break;
+        if (!(ok = wd.wait(&bars.a_full[sl], (s / kASlots) & 1))) break;
         tc_fence_after_sync();
         const uint64_t bd = b_desc0 + static_cast<uint64_t>(st * (kStageBytes >> 4));
-        const uint32_t a = tmem + kColA + 32u * st;
+        const uint32_t a = tmem + kColA + 32u * sl;
 #pragma unroll
         for (int ks = 0; ks < kBK / 16; ++ks)
           umma_bf16_ts(tmem + kColAcc, a + 8u * ks, bd + mnmajor_off(ks), idesc, (s > 0 || ks > 0) ? 1u : 0u);
         umma_commit(&bars.h_empty[st]);
-        umma_commit(&bars.a_empty[st]);
+        umma_commit(&bars.a_empty[sl]);
       }
       if (ok) umma_commit(&bars.acc_full);
       umma_commit(&bars.mma_final);
@@ -162,14 +166,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool j_ok = j < p.n;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     bool ok = true;
-    for (int s = par; s < n_st; s += 2) {
-      const int st = s % kStages;
-      if (!(ok = warp_wait(wd, &bars.a_empty[st], ((s / kStages) & 1) ^ 1))) break;
+    // G of stage s (64 rows of column j) into registers; the loads of the
+    // warp's next stage are issued before the current one is converted, so
+    // two stages of loads per warp are in flight
+    auto load = [&](float (&x)[kBK], int s) {
       const int b = s / p.blocks;
       const int blk = s - b * p.blocks;
       const int valid = min(kBK, p.rows - blk * kBK);   // rows of this stage inside the range
       const float* src = p.g + (static_cast<int64_t>(b) * p.T + p.row_begin + blk * kBK) * p.n + j;
-      float x[kBK];
       if (valid == kBK && j_ok) {
 #pragma unroll
         for (int i = 0; i < kBK; ++i) x[i] = __ldg(src + static_cast<int64_t>(i) * p.n);
@@ -177,13 +181,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kBK; ++i) x[i] = (i < valid && j_ok) ? __ldg(src + static_cast<int64_t>(i) * p.n) : 0.f;
       }
+    };
+    auto put = [&](const float (&x)[kBK], int s) -> bool {
+      const int sl = s % kASlots;
+      if (!warp_wait(wd, &bars.a_empty[sl], ((s / kASlots) & 1) ^ 1)) return false;
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(x[2 * c], x[2 * c + 1]);
-      tmem_st32(tmem + lane_base + kColA + 32u * st, pk);
+      tmem_st32(tmem + lane_base + kColA + 32u * sl, pk);
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&bars.a_full[st]);
+      mbar_arrive(&bars.a_full[sl]);
+      return true;
+    };
+    float x0[kBK], x1[kBK];
+    if (par < n_st) load(x0, par);
+    for (int s = par; s < n_st; s += 4) {
+      if (s + 2 < n_st) load(x1, s + 2);
+      if (!(ok = put(x0, s))) break;
+      if (s + 2 >= n_st) break;
+      if (s + 4 < n_st) load(x0, s + 4);
+      if (!(ok = put(x1, s + 2))) break;
     }
     // ---- epilogue: dW[m0 + c, j] += D[j, c]; warp parity half takes 128 of the 256 columns
     if (ok) ok = warp_wait(wd, &bars.acc_full, 0);
@@ -196,14 +214,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_base + kColAcc + c0, r);
         tmem_ld_wait();
         if (j_ok) {
+          // all 32 loads first, then the stores: a load-add-store per element
+          // would put a global-memory round trip on every column
+          float old[32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int m = m0 + c0 + c;
-            if (m < p.d_model) {
-              float* dst = col + static_cast<int64_t>(m) * p.n;
-              *dst = *dst + __uint_as_float(r[c]);
-            }
-          }
+          for (int c = 0; c < 32; ++c)
+            old[c] = m0 + c0 + c < p.d_model ? col[static_cast<int64_t>(m0 + c0 + c) * p.n] : 0.f;
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (m0 + c0 + c < p.d_model) col[static_cast<int64_t>(m0 + c0 + c) * p.n] = old[c] + __uint_as_float(r[c]);
         }
       }
     }
