@@ -56,10 +56,15 @@ cudaError_t launch_bwd_bf16(const ChunkGeom& g, const Bf16BwdMaps& maps, const f
                             float* dq, float* dk, float* dv, unsigned int* err, cudaStream_t s);
 
 // ---- projection weight gradient (tcgen05, G rounded to bf16 in the kernel) -
-// map_h: 3-D bf16 tensor map over h [batch, seq_len, d_model] with a box of
-// {64 columns, 64 rows, 1 batch entry} and 128-byte swizzle.
-cudaError_t launch_wgrad_bf16(const CUtensorMap& map_h, int32_t batch, int64_t seq_len, int64_t row_begin,
-                              int64_t row_end, int32_t d_model, int32_t n, const float* g, float* dw,
-                              unsigned int* err, long long wait_cycles, cudaStream_t s);
+// h: bf16 [B, T, d_model], box {64 columns, 64 rows, 1}, 128-byte swizzle;
+// g: fp32 [B, T, n], box {128 columns, 64 rows, 1}, no swizzle;
+// dw: fp32 [1, d_model, n], box {128 columns, 32 rows, 1}, no swizzle (the
+// target of the epilogue's reduce-adds).
+struct WgradMaps {
+  CUtensorMap h, g, dw;
+};
+cudaError_t launch_wgrad_bf16(const WgradMaps& maps, int32_t batch, int64_t row_begin, int64_t row_end,
+                              int32_t d_model, int32_t n, unsigned int* err, long long wait_cycles,
+                              cudaStream_t s);
 
 }  // namespace seqattn

@@ -102,19 +102,24 @@ bool make_map(CUtensorMap* m, const void* base, int d, int heads, int64_t rows, 
   return r == CUDA_SUCCESS;
 }
 
-// 3-D bf16 tensor map over a row-major [B, T, cols] tensor: box of {64
-// columns, box_rows rows, 1 batch entry}, 128-byte swizzle.  Rows past T and
-// columns past `cols` read as zero.
-bool make_map_btc(CUtensorMap* m, const void* base, int64_t B, int64_t T, int64_t cols, int box_rows) {
+// 3-D tensor map over a row-major [B, T, cols] tensor of bf16 (128-byte
+// swizzle, box {64 columns, box_rows rows, 1 batch entry}) or float32 (no
+// swizzle, box {box_cols, box_rows, 1}).  Rows past T and columns past
+// `cols` read as zero and are never written.
+bool make_map_btc(CUtensorMap* m, const void* base, int64_t B, int64_t T, int64_t cols, bool fp32,
+                  int box_cols, int box_rows) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   memset(m, 0, sizeof(*m));
+  const cuuint64_t es_bytes = fp32 ? 4 : 2;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, static_cast<cuuint64_t>(T) * static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * es_bytes,
+                           static_cast<cuuint64_t>(T) * static_cast<cuuint64_t>(cols) * es_bytes};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  fp32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -306,10 +311,12 @@ seqattn_status seqattn_proj_wgrad(int32_t batch, int64_t seq_len, int64_t row_be
   unsigned int* err = nullptr;
   cudaError_t e = error_word(&err);
   if (e != cudaSuccess) return cuda_fail(e, "error word");
-  CUtensorMap map_h;
-  if (!make_map_btc(&map_h, h, batch, seq_len, d_model, 64))
-    return fail(SEQATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for h");
-  e = launch_wgrad_bf16(map_h, batch, seq_len, row_begin, row_end, d_model, n, g, dw, err,
+  WgradMaps maps;
+  if (!make_map_btc(&maps.h, h, batch, seq_len, d_model, false, 64, 64) ||
+      !make_map_btc(&maps.g, g, batch, seq_len, n, true, 128, 64) ||
+      !make_map_btc(&maps.dw, dw, 1, d_model, n, true, 128, 32))
+    return fail(SEQATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for h, g or dw");
+  e = launch_wgrad_bf16(maps, batch, row_begin, row_end, d_model, n, err,
                         g_wait_cycles.load(std::memory_order_relaxed), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ok() : cuda_fail(e, "wgrad launch");
 }

@@ -11,19 +11,20 @@
 // (256 of the d_model inputs) and runs the whole row range through it:
 //   D[j, m] = sum_r G[r, j] H[r, m]   (= dW[m, j]),   M = 128 (j), N = 256 (m)
 // as tcgen05 MMAs with the A operand (G^T, bf16 pairs) in tensor memory and
-// the B operand (H, MN-major) in shared memory.  G needs converting, so the
-// converter warps read it straight from global memory (one coalesced 128-byte
-// row segment per warp and row), round it to bf16 pairs and store them into a
-// ring of A slots in TMEM; no converted copy of G ever exists in HBM or
-// shared memory.  H comes in by TMA.
-//   warp 0      TMA producer of H (64 rows x 256 columns per stage, 6 stages)
+// the B operand (H, MN-major) in shared memory.  Both inputs arrive by TMA,
+// 64 rows per stage: H (bf16, 128-byte swizzle) and G (fp32, plain rows).  G
+// needs rounding, so converter warps read their column of the fp32 stage,
+// round it to bf16 pairs and store them into a ring of A slots in TMEM; no
+// converted copy of G exists in HBM.
+//   warp 0      TMA producer (H and G, 3 stages of 64 KB)
 //   warp 1      TMEM owner + MMA issuer (4 MMAs M128 N256 K16 per stage)
 //   warps 2..9  converters, one per TMEM lane quadrant and stage parity; then
-//               the epilogue: dW tile += D (load, add, store: within one call
-//               this CTA is the only writer of the tile)
+//               the epilogue: D is written transposed into shared memory (the
+//               idle stage ring) as dW's [256 m][128 j] tile, and one thread
+//               adds it into dW with TMA reduce-adds, so the read-modify-write
+//               of dW runs in L2, overlapped with the next CTAs' work
 // TMEM (512 columns): the accumulator D in [0, 256), four A slots of 32
-// columns (64 rows as bf16 pairs) in [256, 384).  Each converter warp keeps
-// the loads of its next stage in flight while it converts the current one.
+// columns (64 rows as bf16 pairs) in [256, 384).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -35,32 +36,33 @@ namespace {
 constexpr int kBM = 128;               // dW columns (n) per CTA: the MMA's M
 constexpr int kBN = 256;               // dW rows (d_model) per CTA: the MMA's N
 constexpr int kBK = 64;                // rows (tokens) per stage
-constexpr int kStages = 6;             // shared-memory ring of H
+constexpr int kStages = 3;             // shared-memory ring of H and G
 constexpr int kASlots = 4;             // TMEM ring of converted G
 constexpr int kConvWarps = 8;          // two per TMEM lane quadrant
 constexpr int kThreads = 32 * (2 + kConvWarps);
-constexpr int kBoxBytes = kBK * 128;   // one 64-column block of a stage: 64 rows x 128 B
-constexpr int kStageBytes = (kBN / 64) * kBoxBytes;   // 32 KB
+constexpr int kBoxBytes = kBK * 128;   // one 64-column block of H: 64 rows x 128 B
+constexpr int kHBytes = (kBN / 64) * kBoxBytes;       // 32 KB
+constexpr int kGBytes = kBK * kBM * 4;                // 32 KB: 64 rows x 128 fp32
+constexpr int kStageBytes = kHBytes + kGBytes;
+constexpr int kOutRows = 32;                          // dW rows per TMA reduce box
 constexpr int kSmemAlloc = kStages * kStageBytes + 1024;
+static_assert(kBN * kBM * 4 <= kStages * kStageBytes, "the dW tile is staged in the ring");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColAcc = 0;
 constexpr uint32_t kColA = 256;        // A slot s at kColA + 32 s
 
 struct WgradParams {
   int B;
-  int T;                // rows of h and g per batch entry
   int row_begin;
   int rows;             // row_end - row_begin
   int blocks;           // ceil(rows / 64): stages per batch entry
   int d_model, n;
-  const float* g;       // [B, T, n]
-  float* dw;            // [d_model, n]
   unsigned int* err;
   long long wait_cycles;
 };
 
 struct WgradBarriers {
-  uint64_t h_full[kStages], h_empty[kStages];
+  uint64_t full[kStages], empty[kStages];
   uint64_t a_full[kASlots], a_empty[kASlots];
   uint64_t acc_full;
   uint64_t mma_final;
@@ -76,7 +78,8 @@ __device__ __forceinline__ bool warp_wait(Watchdog& wd, uint64_t* bar, uint32_t 
 __host__ __device__ constexpr uint32_t mnmajor_off(int ks) { return static_cast<uint32_t>((ks * 2048) >> 4); }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    wgrad_bf16_kernel(const __grid_constant__ CUtensorMap map_h, const WgradParams p) {
+    wgrad_bf16_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_g,
+                      const __grid_constant__ CUtensorMap map_dw, const WgradParams p) {
   if (error_already_set(p.err)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -98,8 +101,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&bars.h_full[i], 1);
-      mbar_init(&bars.h_empty[i], 1);
+      mbar_init(&bars.full[i], 1);
+      mbar_init(&bars.empty[i], 1);
     }
     for (int i = 0; i < kASlots; ++i) {
       mbar_init(&bars.a_full[i], 4 * 32);    // the four converter warps of the slot's parity
@@ -122,15 +125,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tensormap(&map_h);
+      prefetch_tensormap(&map_g);
+      prefetch_tensormap(&map_dw);
       for (int s = 0; s < n_st; ++s) {
         const int st = s % kStages;
-        if (!wd.wait(&bars.h_empty[st], ((s / kStages) & 1) ^ 1)) break;
+        if (!wd.wait(&bars.empty[st], ((s / kStages) & 1) ^ 1)) break;
         const int b = s / p.blocks;
         const int r0 = p.row_begin + (s - b * p.blocks) * kBK;
-        mbar_arrive_expect_tx(&bars.h_full[st], kStageBytes);
+        uint8_t* stage = smem + st * kStageBytes;
+        mbar_arrive_expect_tx(&bars.full[st], kStageBytes);
 #pragma unroll
         for (int blk = 0; blk < kBN / 64; ++blk)
-          tma_load_3d(smem + st * kStageBytes + blk * kBoxBytes, &map_h, &bars.h_full[st], m0 + 64 * blk, r0, b);
+          tma_load_3d(stage + blk * kBoxBytes, &map_h, &bars.full[st], m0 + 64 * blk, r0, b);
+        tma_load_3d(stage + kHBytes, &map_g, &bars.full[st], n0, r0, b);
         n_issued = s + 1;
       }
     }
@@ -143,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; ok && s < n_st; ++s) {
         const int st = s % kStages;
         const int sl = s % kASlots;
-        if (!(ok = wd.wait(&bars.h_full[st], (s / kStages) & 1))) break;
+        if (!(ok = wd.wait(&bars.full[st], (s / kStages) & 1))) break;
         if (!(ok = wd.wait(&bars.a_full[sl], (s / kASlots) & 1))) break;
         tc_fence_after_sync();
         const uint64_t bd = b_desc0 + static_cast<uint64_t>(st * (kStageBytes >> 4));
@@ -151,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < kBK / 16; ++ks)
           umma_bf16_ts(tmem + kColAcc, a + 8u * ks, bd + mnmajor_off(ks), idesc, (s > 0 || ks > 0) ? 1u : 0u);
-        umma_commit(&bars.h_empty[st]);
+        umma_commit(&bars.empty[st]);         // H and G of the stage consumed (G before a_full)
         umma_commit(&bars.a_empty[sl]);
       }
       if (ok) umma_commit(&bars.acc_full);
@@ -162,80 +169,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ converters
     const int quad = warp & 3;
     const int par = (warp - 2) >> 2;                    // stages s with s % 2 == par
-    const int j = n0 + quad * 32 + lane;                // dW column (TMEM lane) of this thread
-    const bool j_ok = j < p.n;
+    const int jl = quad * 32 + lane;                    // tile column (TMEM lane) of this thread
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     bool ok = true;
-    // G of stage s (64 rows of column j) into registers; the loads of the
-    // warp's next stage are issued before the current one is converted, so
-    // two stages of loads per warp are in flight
-    auto load = [&](float (&x)[kBK], int s) {
+    for (int s = par; s < n_st; s += 2) {
+      const int st = s % kStages;
+      const int sl = s % kASlots;
+      if (!(ok = warp_wait(wd, &bars.a_empty[sl], ((s / kASlots) & 1) ^ 1))) break;
+      if (!(ok = warp_wait(wd, &bars.full[st], (s / kStages) & 1))) break;
       const int b = s / p.blocks;
-      const int blk = s - b * p.blocks;
-      const int valid = min(kBK, p.rows - blk * kBK);   // rows of this stage inside the range
-      const float* src = p.g + (static_cast<int64_t>(b) * p.T + p.row_begin + blk * kBK) * p.n + j;
-      if (valid == kBK && j_ok) {
+      const int valid = min(kBK, p.rows - (s - b * p.blocks) * kBK);   // rows inside the range
+      // this thread's column of the fp32 stage: 64 rows, 128 floats apart
+      // (lanes read consecutive words, no bank conflicts); rows past the
+      // range become zeros, so whatever H holds there adds nothing
+      const float* gs = reinterpret_cast<const float*>(smem + st * kStageBytes + kHBytes) + jl;
+      uint32_t pk[32];
+      if (valid == kBK) {
 #pragma unroll
-        for (int i = 0; i < kBK; ++i) x[i] = __ldg(src + static_cast<int64_t>(i) * p.n);
+        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(gs[(2 * c) * kBM], gs[(2 * c + 1) * kBM]);
       } else {
 #pragma unroll
-        for (int i = 0; i < kBK; ++i) x[i] = (i < valid && j_ok) ? __ldg(src + static_cast<int64_t>(i) * p.n) : 0.f;
+        for (int c = 0; c < 32; ++c)
+          pk[c] = pack_bf16x2(2 * c < valid ? gs[(2 * c) * kBM] : 0.f, 2 * c + 1 < valid ? gs[(2 * c + 1) * kBM] : 0.f);
       }
-    };
-    auto put = [&](const float (&x)[kBK], int s) -> bool {
-      const int sl = s % kASlots;
-      if (!warp_wait(wd, &bars.a_empty[sl], ((s / kASlots) & 1) ^ 1)) return false;
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(x[2 * c], x[2 * c + 1]);
       tmem_st32(tmem + lane_base + kColA + 32u * sl, pk);
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(&bars.a_full[sl]);
-      return true;
-    };
-    float x0[kBK], x1[kBK];
-    if (par < n_st) load(x0, par);
-    for (int s = par; s < n_st; s += 4) {
-      if (s + 2 < n_st) load(x1, s + 2);
-      if (!(ok = put(x0, s))) break;
-      if (s + 2 >= n_st) break;
-      if (s + 4 < n_st) load(x0, s + 4);
-      if (!(ok = put(x1, s + 2))) break;
     }
-    // ---- epilogue: dW[m0 + c, j] += D[j, c]; warp parity half takes 128 of the 256 columns
+    // ---- epilogue: once every MMA has completed the stage ring is idle (all
+    // issued copies were consumed); D goes there transposed, as the dW tile
+    // [256 m][128 j] fp32, this warp pair's half of the m rows each
     if (ok) ok = warp_wait(wd, &bars.acc_full, 0);
     if (ok) {
       tc_fence_after_sync();
-      float* col = p.dw + j;
+      float* out = reinterpret_cast<float*>(smem);
 #pragma unroll 1
       for (int c0 = par * (kBN / 2); c0 < (par + 1) * (kBN / 2); c0 += 32) {
         uint32_t r[32];
         tmem_ld32(tmem + lane_base + kColAcc + c0, r);
         tmem_ld_wait();
-        if (j_ok) {
-          // all 32 loads first, then the stores: a load-add-store per element
-          // would put a global-memory round trip on every column
-          float old[32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            old[c] = m0 + c0 + c < p.d_model ? col[static_cast<int64_t>(m0 + c0 + c) * p.n] : 0.f;
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (m0 + c0 + c < p.d_model) col[static_cast<int64_t>(m0 + c0 + c) * p.n] = old[c] + __uint_as_float(r[c]);
-        }
+        for (int c = 0; c < 32; ++c) out[(c0 + c) * kBM + jl] = __uint_as_float(r[c]);
       }
+      fence_proxy_async_smem();
+    }
+    named_barrier_sync(1, kConvWarps * 32);
+    if (ok && !wd.aborted() && warp == 2 && lane == 0) {
+      // dW rows [m0, m0 + 256) x columns [n0, n0 + 128) += the staged tile;
+      // the parts past d_model or n are clipped by the tensor map
+#pragma unroll 1
+      for (int k = 0; k < kBN / kOutRows; ++k)
+        tma_reduce_add_3d(&map_dw, smem + k * kOutRows * kBM * 4, n0, m0 + k * kOutRows, 0);
+      bulk_commit_group();
+      bulk_wait_group_read<0>();            // the tile has been read before the CTA's smem goes away
     }
   }
 
   tc_fence_before_sync();
   __syncthreads();
   if (wd.aborted()) {
-    // a wait ran out: let the H copies already in flight land first
+    // a wait ran out: let the copies already in flight land first
     if (warp == 0 && lane == 0) {
       for (int st = 0; st < kStages && st < n_issued; ++st) {
         const int last = st + kStages * ((n_issued - 1 - st) / kStages);
-        wd.drain(&bars.h_full[st], (last / kStages) & 1, 1000000);
+        wd.drain(&bars.full[st], (last / kStages) & 1, 1000000);
       }
     }
     __syncthreads();
@@ -248,25 +246,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_wgrad_bf16(const CUtensorMap& map_h, int32_t batch, int64_t seq_len, int64_t row_begin,
-                              int64_t row_end, int32_t d_model, int32_t n, const float* g, float* dw,
-                              unsigned int* err, long long wait_cycles, cudaStream_t s) {
+cudaError_t launch_wgrad_bf16(const WgradMaps& maps, int32_t batch, int64_t row_begin, int64_t row_end,
+                              int32_t d_model, int32_t n, unsigned int* err, long long wait_cycles,
+                              cudaStream_t s) {
   WgradParams p;
   p.B = batch;
-  p.T = static_cast<int>(seq_len);
   p.row_begin = static_cast<int>(row_begin);
   p.rows = static_cast<int>(row_end - row_begin);
   p.blocks = (p.rows + kBK - 1) / kBK;
   p.d_model = d_model;
   p.n = n;
-  p.g = g;
-  p.dw = dw;
   p.err = err;
   p.wait_cycles = wait_cycles;
   cudaError_t e = cudaFuncSetAttribute(wgrad_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(((n + kBM - 1) / kBM) * ((d_model + kBN - 1) / kBN));
-  wgrad_bf16_kernel<<<grid, kThreads, kSmemAlloc, s>>>(map_h, p);
+  wgrad_bf16_kernel<<<grid, kThreads, kSmemAlloc, s>>>(maps.h, maps.g, maps.dw, p);
   return cudaGetLastError();
 }
 
