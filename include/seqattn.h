@@ -104,10 +104,11 @@ seqattn_status seqattn_chunk_fwd(const seqattn_problem* pb, int64_t q_start, int
  *   workspace: device scratch of at least seqattn_bwd_workspace_size(pb,
  *     q_len) bytes, 256-byte aligned, caller-owned, contents not preserved.
  * Size rules as for seqattn_chunk_fwd.  Calls on one stream accumulate in
- * order.  SEQATTN_BF16: the accumulator updates are fp32 atomic adds, so calls
- * for different chunks may run concurrently on different streams, each with a
- * workspace of its own (the order of the fp32 additions, and so the last bits
- * of the sums, then varies between runs).  SEQATTN_FP32: the updates are
+ * order.  SEQATTN_BF16: the accumulator updates are fp32 reduce-adds done in
+ * L2 (atomic per element), so calls for different chunks may run concurrently
+ * on different streams, each with a workspace of its own (the order of the
+ * fp32 additions, and so the last bits of the sums, then varies between
+ * runs).  SEQATTN_FP32: the updates are
  * plain read-modify-writes; two calls that update the same accumulator rows
  * must not run concurrently.
  */

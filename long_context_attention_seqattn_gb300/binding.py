@@ -446,8 +446,8 @@ def layer_forward_backward(q, k, v, d_o, chunk, scale=None, bufs=None, stream=No
     its dK/dV rows are final (every later chunk has run), so
     dw_x += H^(i)T dX^(i) is added for each of the three (h: [B, T, d_model]
     bf16; dw_q: [d_model, Hq d], dw_k, dw_v: [d_model, Hkv d], float32,
-    accumulated).  Needs the descending order.  With more than one backward
-    stream they run on a relay stream that waits until each chunk's rows are
+    accumulated).  Needs the descending order.  They run on three relay
+    streams (one per projection) that wait until each chunk's rows are
     final."""
     B, T, Hq, d = q.shape
     if bufs is None:
@@ -460,23 +460,26 @@ def layer_forward_backward(q, k, v, d_o, chunk, scale=None, bufs=None, stream=No
         bwd_streams = auto_bwd_streams(q, k, chunk)
     main = stream if stream is not None else torch.cuda.current_stream()
     on_final = None
-    relay = main
+    relays = []
     if wgrad is not None:
-        if bwd_streams > 1:
-            relay = side_streams(q.device, bwd_streams)[bwd_streams - 1]
-            relay.wait_stream(main)
+        # one relay stream per projection (after the backward's side streams):
+        # the three weight gradients of a chunk run side by side, and beside
+        # the backwards of the earlier chunks; each dW is updated in chunk
+        # order on its own stream
+        relays = side_streams(q.device, bwd_streams + 2)[bwd_streams - 1:]
+        for r in relays:
+            r.wait_stream(main)
 
         def on_final(i, s, e, events):
             h, dw_q, dw_k, dw_v = wgrad
-            if relay is not main:
+            for r, (g, dw) in zip(relays, ((bufs.dq, dw_q), (bufs.dk, dw_k), (bufs.dv, dw_v))):
                 for ev in events:
-                    relay.wait_event(ev)
-            for g, dw in ((bufs.dq, dw_q), (bufs.dk, dw_k), (bufs.dv, dw_v)):
-                proj_wgrad(h, g, dw, s, e, relay)
+                    r.wait_event(ev)
+                proj_wgrad(h, g, dw, s, e, r)
 
     backward_chunks(q, k, v, d_o, chunk, bufs, scale, main, bwd_streams, bwd_order, on_final)
-    if relay is not main:
-        main.wait_stream(relay)
+    for r in relays:
+        main.wait_stream(r)
     return bufs
 
 

@@ -12,11 +12,12 @@
 // One CTA owns one 128-key tile of one key/value head: it loops over the G
 // query heads of the group and the chunk's 64-row query tiles that can see the
 // tile ("steps"), keeps dK and dV for its 128 keys in TMEM for the whole loop,
-// and finally adds them into the float32 accumulators with vector fp32
-// reductions (16-byte atomic adds carried out in L2).  Within one call no other
-// CTA touches those rows, so the reductions meet no contention; they need no
-// load of the old sums, and backward calls of different chunks may run
-// concurrently on different streams.  dQ partial products of every key tile
+// and finally stages them in shared memory and adds them into the float32
+// accumulators with TMA reduce-adds (bulk fp32 additions carried out in L2,
+// atomic per element).  Within one call no other CTA touches those rows, so
+// the reductions meet no contention; they need no load of the old sums, and
+// backward calls of different chunks may run concurrently on different
+// streams.  dQ partial products of every key tile
 // are summed into the zeroed dq with fp32 reductions.  Chunks may start
 // and end anywhere: a partial last query tile reads padding statistics
 // (-inf, 0) that make its extra rows' P exactly 0, and rows past the chunk
@@ -38,8 +39,8 @@
 //                dQ^T = K^T dS^T (M=128 rows of d, zero-padded when d = 64;
 //                N=64, K=128; SS)
 //   warps 2..9   P^T, then dS^T: two warps per TMEM lane quadrant, 32 query
-//                columns each; dS^T also to shared memory for dQ^T; the final
-//                dK (warps 2-5) / dV (6-9) reductions
+//                columns each; dS^T also to shared memory for dQ^T; at the
+//                end dK (warps 2-5) / dV (6-9) staged for the reduce-adds
 //   warps 10..13 dQ^T from TMEM -> fp32 reductions into dq
 // Three issuing threads because one thread keeps only about one tcgen05.mma
 // in flight per ~90 cycles, whatever its shape; S^T and dP^T, which gate the
@@ -83,6 +84,7 @@ struct BwdCfg {
   static constexpr int kOffStat = kOffDS + 2 * kPTileBytes;   // kQStages x (-L log2 e [64], Delta [64])
   static constexpr int kSmemBytes = kOffStat + kQStages * kStatBytes;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;
+  static_assert(2 * kBK * D * 4 <= kOffStat - kOffQ, "dK and dV are staged in the Q/dO ring and dS buffers");
 };
 
 constexpr uint32_t kTmemCols = 512;
@@ -168,6 +170,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_bf16_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                    const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
                     const BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int kDQWarps = D / 32;                   // dQ warps holding live d rows of dQ^T
@@ -199,7 +202,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     g = j - (j / p.Hkv) * p.Hkv;
   }
   const int kb = p.kv_begin + kt * kBK;                  // absolute first key of the tile
-  const int q_end = p.q_start + p.q_len;                 // one past the chunk's last row
   // first query tile that sees any key of this tile (the one holding row kb)
   const int qi_first = kb > p.q_start ? (kb - p.q_start) / kBQ : 0;
   const int nq = p.n_q64 - qi_first;
@@ -456,31 +458,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (++qi == qi_first + nq) qi = qi_first;
     }
-    // ---- epilogue: this tile's dK (half 0) or dV (half 1) rows into the running sums
+    // ---- epilogue: this tile's dK (half 0) and dV (half 1) go to shared
+    // memory (the idle Q/dO ring) as 128-row boxes of 32 columns with the
+    // 128-byte swizzle, then one thread adds them into the running sums with
+    // TMA reduce-adds; rows past the chunk's end are cut by the tensor maps
     if (ok) ok = warp_wait(wd, &bars.acc_done, 0);
     if (ok) {                                           // warp-uniform: the TMEM loads are .sync.aligned
       tc_fence_after_sync();
-      const bool store = key < q_end;                   // keys of a partial last tile past the chunk are dropped
-      const int64_t row = (static_cast<int64_t>(b) * p.T + key) * p.Hkv + g;
-      float4* dst = reinterpret_cast<float4*>((half == 0 ? p.dk : p.dv) + row * D);
       const uint32_t col = half == 0 ? kColDK : kColDV;
       const float f = half == 0 ? p.scale : 1.f;
+      uint8_t* stage = smem + C::kOffQ + half * (D / 32) * 16384;
+      const uint32_t sw = static_cast<uint32_t>(kr & 7);
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 64) {
-        uint32_t r0[32], r1[32];
-        tmem_ld32(tmem + lane_base + col + c0, r0);
-        tmem_ld32(tmem + lane_base + col + c0 + 32, r1);
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_base + col + c0, r);
         tmem_ld_wait();
+        const uint32_t rowa = smem_u32(stage + (c0 / 32) * 16384 + kr * 128);
 #pragma unroll
-        for (int j = 0; j < 32 && store; j += 4)
-          atomicAdd(dst + (c0 + j) / 4, make_float4(f * __uint_as_float(r0[j]), f * __uint_as_float(r0[j + 1]),
-                                                    f * __uint_as_float(r0[j + 2]), f * __uint_as_float(r0[j + 3])));
-#pragma unroll
-        for (int j = 0; j < 32 && store; j += 4)
-          atomicAdd(dst + (c0 + 32 + j) / 4,
-                    make_float4(f * __uint_as_float(r1[j]), f * __uint_as_float(r1[j + 1]),
-                                f * __uint_as_float(r1[j + 2]), f * __uint_as_float(r1[j + 3])));
+        for (int c4 = 0; c4 < 8; ++c4)
+          st_shared_v4(rowa + ((c4 ^ sw) << 4), __float_as_uint(f * __uint_as_float(r[4 * c4])),
+                       __float_as_uint(f * __uint_as_float(r[4 * c4 + 1])),
+                       __float_as_uint(f * __uint_as_float(r[4 * c4 + 2])),
+                       __float_as_uint(f * __uint_as_float(r[4 * c4 + 3])));
       }
+      fence_proxy_async_smem();
+    }
+    named_barrier_sync(2, kComputeWarps * 32);
+    if (ok && !wd.aborted() && warp == 2 && lane == 0) {
+#pragma unroll 1
+      for (int bx = 0; bx < D / 32; ++bx) {
+        tma_reduce_add_4d(&map_dk, smem + C::kOffQ + bx * 16384, 32 * bx, g, kb, b);
+        tma_reduce_add_4d(&map_dv, smem + C::kOffQ + (D / 32 + bx) * 16384, 32 * bx, g, kb, b);
+      }
+      bulk_commit_group();
+      bulk_wait_group_read<0>();
     }
   } else {
     // ------------------------------------------------------------ dQ
@@ -548,7 +560,8 @@ cudaError_t launch_bwd_bf16_d(const BwdParams& p, const Bf16BwdMaps& maps, unsig
   cudaError_t e = cudaFuncSetAttribute(bwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        BwdCfg<D>::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  bwd_bf16_kernel<D><<<grid, kThreads, BwdCfg<D>::kSmemAlloc, s>>>(maps.q, maps.k, maps.v, maps.d_o, p);
+  bwd_bf16_kernel<D><<<grid, kThreads, BwdCfg<D>::kSmemAlloc, s>>>(maps.q, maps.k, maps.v, maps.d_o, maps.dk,
+                                                                     maps.dv, p);
   return cudaGetLastError();
 }
 

@@ -48,6 +48,7 @@ struct Bf16FwdMaps {
 };
 struct Bf16BwdMaps {
   CUtensorMap q, k, v, d_o;
+  CUtensorMap dk, dv;   // fp32 [B][rows < q_end][Hkv][d], box {32, 1, 128, 1}, 128-byte swizzle
 };
 cudaError_t launch_fwd_bf16(const ChunkGeom& g, const Bf16FwdMaps& maps, void* o, float* lse,
                             unsigned int* err, cudaStream_t s);

@@ -124,6 +124,25 @@ bool make_map_btc(CUtensorMap* m, const void* base, int64_t B, int64_t T, int64_
   return r == CUDA_SUCCESS;
 }
 
+// 4-D float32 tensor map over the [B, T, heads, d] accumulator, cut at row
+// `rows` of every batch entry (the chunk's end: rows past it are never
+// written): box {32 of d, 1 head, 128 rows, 1 batch entry}, 128-byte swizzle.
+bool make_map_accum(CUtensorMap* m, const void* base, int d, int heads, int64_t T, int64_t rows, int B) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  memset(m, 0, sizeof(*m));
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(heads) * d * 4,
+                           static_cast<cuuint64_t>(T) * heads * d * 4};
+  cuuint32_t box[4] = {32, 1, 128, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 seqattn_status check_problem(const seqattn_problem* pb) {
@@ -257,7 +276,9 @@ seqattn_status seqattn_chunk_bwd(const seqattn_problem* pb, int64_t q_start, int
   if (!make_map(&maps.q, q, g.d, g.Hq, static_cast<int64_t>(g.B) * q_len, 64) ||
       !make_map(&maps.d_o, d_o, g.d, g.Hq, static_cast<int64_t>(g.B) * q_len, 64) ||
       !make_map(&maps.k, k, g.d, g.Hkv, static_cast<int64_t>(g.B) * g.T, 128) ||
-      !make_map(&maps.v, v, g.d, g.Hkv, static_cast<int64_t>(g.B) * g.T, 128))
+      !make_map(&maps.v, v, g.d, g.Hkv, static_cast<int64_t>(g.B) * g.T, 128) ||
+      !make_map_accum(&maps.dk, dk_accum, g.d, g.Hkv, g.T, q_start + q_len, g.B) ||
+      !make_map_accum(&maps.dv, dv_accum, g.d, g.Hkv, g.T, q_start + q_len, g.B))
     return fail(SEQATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the backward operands");
   e = launch_bwd_stats_bf16(g, o, d_o, lse, delta, dq, st);
   if (e != cudaSuccess) return cuda_fail(e, "bwd_stats launch");
@@ -440,7 +461,9 @@ extern "C" seqattn_status seqattn_chunk_bwd_noalloc(
   if (!make_map(&maps.q, q, g.d, g.Hq, static_cast<int64_t>(g.B) * q_len, 64) ||
       !make_map(&maps.d_o, d_o, g.d, g.Hq, static_cast<int64_t>(g.B) * q_len, 64) ||
       !make_map(&maps.k, k, g.d, g.Hkv, static_cast<int64_t>(g.B) * g.T, 128) ||
-      !make_map(&maps.v, v, g.d, g.Hkv, static_cast<int64_t>(g.B) * g.T, 128))
+      !make_map(&maps.v, v, g.d, g.Hkv, static_cast<int64_t>(g.B) * g.T, 128) ||
+      !make_map_accum(&maps.dk, dk_accum, g.d, g.Hkv, g.T, q_start + q_len, g.B) ||
+      !make_map_accum(&maps.dv, dv_accum, g.d, g.Hkv, g.T, q_start + q_len, g.B))
     return fail(SEQATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the backward operands");
   e = launch_bwd_stats_bf16(g, o, d_o, lse, delta, dq, st);
   if (e != cudaSuccess) return cuda_fail(e, "bwd_stats launch");
