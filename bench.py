@@ -427,18 +427,19 @@ def run_ours(args, w):
         dws = [torch.zeros((dm, n), device=dev) for n in (w.hq * w.head_dim, w.hkv * w.head_dim,
                                                          w.hkv * w.head_dim)]
 
-        wstreams = binding.side_streams(dev, n_bwd + 2)[n_bwd - 1:]
+        wstreams = binding.side_streams(dev, n_bwd + 5)[n_bwd - 1:]
 
         def wgrad_pass():
-            # the relay's schedule: one stream per projection, chunks last to
-            # first on each, forked from and joined into the main stream
+            # the relay's schedule (binding.layer_forward_backward): chunks
+            # last to first, two streams per projection taken by alternate
+            # chunks, forked from and joined into the main stream
             for r in wstreams:
                 r.wait_stream(main)
-            for i in range(D - 1, -1, -1):
+            for n, i in enumerate(range(D - 1, -1, -1)):
                 s = starts[i]
                 e = min(s + c, T)
-                for r, g, dw in zip(wstreams, (bufs.dq, bufs.dk, bufs.dv), dws):
-                    binding.proj_wgrad(h, g, dw, s, e, r)
+                for x, (g, dw) in enumerate(zip((bufs.dq, bufs.dk, bufs.dv), dws)):
+                    binding.proj_wgrad(h, g, dw, s, e, wstreams[2 * x + n % 2])
             for r in wstreams:
                 main.wait_stream(r)
 
@@ -457,7 +458,7 @@ def run_ours(args, w):
         wgrad = {"metric": "projection weight-gradient TFLOP/s (dW_q, dW_k, dW_v of one pass)",
                  "value": wg_flops / (wg_ms / 1e3) / 1e12, "unit": UNIT, "ms_per_pass": wg_ms,
                  "d_model": dm, "kernels": "wgrad_bf16_kernel (tcgen05, g rounded to bf16 in the kernel, float32 accumulate)",
-                 "streams": "dQ, dK, dV projections on three streams, each in chunk order",
+                 "streams": "the relay's schedule: two streams per projection, alternate chunks",
                  "launches_per_pass": 3 * D}
         del h, dws
 

@@ -184,8 +184,9 @@ seqattn_status seqattn_scale_accum_rows(const seqattn_problem* pb, int64_t row_b
  *   dw: [d_model, n] float32, row-major, accumulated (never overwritten)
  * One tensor-core kernel: g is rounded to bf16 (nearest even) as it is read,
  * the products are summed in float32 and each CTA adds its tile into dw with
- * TMA reduce-adds; two calls that update the same dw must not run
- * concurrently (calls on one stream are ordered).  Rows of h outside
+ * TMA reduce-adds (atomic per element in L2), so calls that update the same
+ * dw may run concurrently on different streams (the order of the fp32
+ * additions, and so the last bits of dw, then varies between runs).  Rows of h outside
  * [row_begin, row_end) are read only where they meet a zero of g and must be
  * finite.  Requires batch >= 1, 0 <= row_begin <= row_end <= seq_len,
  * d_model and n positive multiples of 8, and 16-byte aligned pointers.  No

@@ -277,6 +277,13 @@ def _rows(t, s, e):
     return v if v.is_contiguous() else v.contiguous()
 
 
+def _copy_rows(dst, src, s, e):
+    """Asynchronous copy of rows [s, e) of [B, T, ...] tensors between host and
+    device, one contiguous block per batch entry."""
+    for b in range(dst.shape[0]):
+        dst[b, s:e].copy_(src[b, s:e], non_blocking=True)
+
+
 _side_streams = {}
 
 
@@ -446,9 +453,9 @@ def layer_forward_backward(q, k, v, d_o, chunk, scale=None, bufs=None, stream=No
     its dK/dV rows are final (every later chunk has run), so
     dw_x += H^(i)T dX^(i) is added for each of the three (h: [B, T, d_model]
     bf16; dw_q: [d_model, Hq d], dw_k, dw_v: [d_model, Hkv d], float32,
-    accumulated).  Needs the descending order.  They run on three relay
-    streams (one per projection) that wait until each chunk's rows are
-    final."""
+    accumulated).  Needs the descending order.  They run on six relay
+    streams (two per projection, alternate chunks) that wait until each
+    chunk's rows are final."""
     B, T, Hq, d = q.shape
     if bufs is None:
         bufs = LayerBuffers(q, k, chunk)
@@ -462,17 +469,22 @@ def layer_forward_backward(q, k, v, d_o, chunk, scale=None, bufs=None, stream=No
     on_final = None
     relays = []
     if wgrad is not None:
-        # one relay stream per projection (after the backward's side streams):
-        # the three weight gradients of a chunk run side by side, and beside
-        # the backwards of the earlier chunks; each dW is updated in chunk
-        # order on its own stream
-        relays = side_streams(q.device, bwd_streams + 2)[bwd_streams - 1:]
+        # relay streams after the backward's side streams: two per projection,
+        # taken by alternate chunks, so the three weight gradients of a chunk
+        # run side by side, beside those of the previous chunk and beside the
+        # backwards of the earlier chunks (a dW's reduce-adds are atomic per
+        # element, so two chunks may update it at once)
+        relays = side_streams(q.device, bwd_streams + 5)[bwd_streams - 1:]
         for r in relays:
             r.wait_stream(main)
+        seen = [0]
 
         def on_final(i, s, e, events):
             h, dw_q, dw_k, dw_v = wgrad
-            for r, (g, dw) in zip(relays, ((bufs.dq, dw_q), (bufs.dk, dw_k), (bufs.dv, dw_v))):
+            par = seen[0] % 2
+            seen[0] += 1
+            for x, (g, dw) in enumerate(((bufs.dq, dw_q), (bufs.dk, dw_k), (bufs.dv, dw_v))):
+                r = relays[2 * x + par]
                 for ev in events:
                     r.wait_event(ev)
                 proj_wgrad(h, g, dw, s, e, r)
@@ -576,8 +588,6 @@ class HostLayerPass:
 
     def __init__(self, h_q, h_k, h_v, h_do, chunk, device="cuda"):
         B, T, Hq, d = h_q.shape
-        if B != 1:
-            raise ValueError("HostLayerPass streams row ranges of B=1 tensors")
         self.h_in = (h_q, h_k, h_v, h_do)
         self.chunk = chunk
         self.d_in = tuple(torch.empty(x.shape, dtype=x.dtype, device=device) for x in self.h_in)
@@ -613,7 +623,7 @@ class HostLayerPass:
             for s in starts:
                 e = min(s + c, T)
                 for dst, src in ((q, h_q), (k, h_k), (v, h_v)):
-                    dst[:, s:e].copy_(src[:, s:e], non_blocking=True)
+                    _copy_rows(dst, src, s, e)
                 ev = torch.cuda.Event()
                 ev.record(self.up)
                 ev_in.append(ev)
@@ -623,7 +633,7 @@ class HostLayerPass:
             for i in range(len(starts) - 1, -1, -1):
                 s = starts[i]
                 e = min(s + c, T)
-                do[:, s:e].copy_(h_do[:, s:e], non_blocking=True)
+                _copy_rows(do, h_do, s, e)
                 ev = torch.cuda.Event()
                 ev.record(self.up)
                 ev_do[i] = ev
@@ -635,12 +645,17 @@ class HostLayerPass:
             e = min(s + c, T)
             st = main if i % 2 == 0 else side
             st.wait_event(ev_in[i])
-            chunk_fwd(_rows(q, s, e), k, v, b.o[:, s:e], b.lse_chunks[i], s, s, None, st)
+            with torch.cuda.stream(st):      # row gathers of a batched chunk on its own stream
+                o_c = b.o[:, s:e]
+                tgt = o_c if o_c.is_contiguous() else torch.empty_like(o_c.contiguous())
+                chunk_fwd(_rows(q, s, e), k, v, tgt, b.lse_chunks[i], s, s, None, st)
+                if tgt is not o_c:
+                    o_c.copy_(tgt)
             ev = torch.cuda.Event()
             ev.record(st)
             self.down.wait_event(ev)
             with torch.cuda.stream(self.down):
-                self.h_o[:, s:e].copy_(b.o[:, s:e], non_blocking=True)
+                _copy_rows(self.h_o, b.o, s, e)
                 self.h_lse[i].copy_(b.lse_chunks[i], non_blocking=True)
         main.wait_stream(side)
 
@@ -653,9 +668,8 @@ class HostLayerPass:
             for ev in events:
                 self.down.wait_event(ev)
             with torch.cuda.stream(self.down):
-                self.h_dq[:, s:e].copy_(b.dq[:, s:e], non_blocking=True)
-                self.h_dk[:, s:e].copy_(b.dk[:, s:e], non_blocking=True)
-                self.h_dv[:, s:e].copy_(b.dv[:, s:e], non_blocking=True)
+                for dst, src in ((self.h_dq, b.dq), (self.h_dk, b.dk), (self.h_dv, b.dv)):
+                    _copy_rows(dst, src, s, e)
 
         backward_chunks(q, k, v, do, c, b, None, main, self.bwd_streams, "descending", on_final, before_chunk)
         main.wait_stream(self.down)

@@ -6,7 +6,8 @@ already issued complete, frees its tensor memory and returns; the host reads
 the word with seqattn_sync_status(), which reports SEQATTN_ERR_TIMEOUT once
 and clears it.  A wait limit of one cycle (seqattn_set_wait_limit) makes every
 wait that is not already complete at its first poll run out, so a normal,
-valid chunk call exercises that path without any fault.  Afterwards the
+valid call (a chunk forward and backward, a projection weight gradient)
+exercises that path without any fault.  Afterwards the
 default limit is restored and the same calls must succeed and match the
 oracle again.
 """
@@ -80,3 +81,34 @@ def test_waits_run_out_report_timeout_then_recover(d):
                                 rdk, rdv)
     for name, a, r in (("O", o, ro), ("LSE", lse, rl), ("dQ", dq, rdq), ("dK", dk, rdk), ("dV", dv, rdv)):
         _close(name, a, r)
+
+
+def test_weight_gradient_waits_run_out_then_recover():
+    """The same for the projection weight-gradient kernel: with a one-cycle
+    limit its waits run out and the status says so once; with the default
+    limit it matches the oracle again."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    lib = binding.load_library()
+    B, T, dm, n, r0, r1 = 1, 512, 256, 256, 64, 448
+    h = inputs.draw("h", 7, B, T, 1, dm, torch.bfloat16)[:, :, 0].contiguous()
+    g = inputs.draw("do", 7, B, T, 1, n, torch.float32)[:, :, 0].contiguous()
+    hd, gd = h.cuda(), g.cuda()
+    dw = torch.zeros((dm, n), device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.seqattn_sync_status(stream) == binding.SEQATTN_OK
+    try:
+        binding.set_wait_limit(1)
+        binding.proj_wgrad(hd, gd, dw, r0, r1)
+        assert lib.seqattn_sync_status(stream) == binding.SEQATTN_ERR_TIMEOUT
+        assert lib.seqattn_sync_status(stream) == binding.SEQATTN_OK
+    finally:
+        binding.set_wait_limit(0)
+    dw.zero_()
+    binding.proj_wgrad(hd, gd, dw, r0, r1)
+    assert lib.seqattn_sync_status(stream) == binding.SEQATTN_OK
+    ref = oracle.projection_wgrad(h[:, r0:r1].double().numpy(), g[:, r0:r1].double().numpy())
+    got = dw.double().cpu().numpy()
+    rel = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    assert rel <= BF16_REL, f"dW after the timeout: rel-L2 {rel:.3e}"
