@@ -307,6 +307,7 @@ def assert_wgrad(name, got, ref):
     (2, 300, 96, 136, 37, 261),        # partial tiles everywhere: 224 rows, 96 of 256 d_model, 136 of 2 x 128 n
     (1, 4096, 4096, 1024, 2048, 4096),  # a dK/dV-shaped chunk of the 32768-token layer's projections
     (1, 1024, 640, 392, 0, 1000),      # 2.5 d_model tiles, 3 + 1/16 n tiles, ragged last stage
+    (2, 700, 512, 200, 13, 650),       # two d_model tiles, a partial n tile, ragged rows, batch 2
 ])
 def test_proj_wgrad_accumulates_h_transpose_g(B, T, dm, n, r0, r1):
     """dw += h^T g over a row range of every batch entry, twice (accumulation

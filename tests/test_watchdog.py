@@ -83,15 +83,16 @@ def test_waits_run_out_report_timeout_then_recover(d):
         _close(name, a, r)
 
 
-def test_weight_gradient_waits_run_out_then_recover():
-    """The same for the projection weight-gradient kernel: with a one-cycle
-    limit its waits run out and the status says so once; with the default
-    limit it matches the oracle again."""
+@pytest.mark.parametrize("dm", [256, 512])
+def test_weight_gradient_waits_run_out_then_recover(dm):
+    """The same for the projection weight-gradient kernel (one and two d_model
+    tiles): with a one-cycle limit its waits run out and the status says so
+    once; with the default limit it matches the oracle again."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     build.build()
     lib = binding.load_library()
-    B, T, dm, n, r0, r1 = 1, 512, 256, 256, 64, 448
+    B, T, n, r0, r1 = 1, 512, 256, 64, 448
     h = inputs.draw("h", 7, B, T, 1, dm, torch.bfloat16)[:, :, 0].contiguous()
     g = inputs.draw("do", 7, B, T, 1, n, torch.float32)[:, :, 0].contiguous()
     hd, gd = h.cuda(), g.cuda()
