@@ -277,6 +277,12 @@ def _rows(t, s, e):
     return v if v.is_contiguous() else v.contiguous()
 
 
+def _nvtx(name):
+    """An NVTX range around one chunk call (host side; it names the call in a
+    profiler's timeline and costs nothing measurable when none is attached)."""
+    return torch.cuda.nvtx.range(name)
+
+
 def _copy_rows(dst, src, s, e):
     """Asynchronous copy of rows [s, e) of [B, T, ...] tensors between host and
     device, one contiguous block per batch entry."""
@@ -327,7 +333,7 @@ def forward_chunks(q, k, v, chunk, bufs, scale=None, stream=None, fwd_streams=No
         st = main if i % fwd_streams == 0 else sides[i % fwd_streams - 1]
         # the row gathers of a batched chunk (B > 1) and their temporaries
         # belong to the chunk's own stream
-        with torch.cuda.stream(st):
+        with torch.cuda.stream(st), _nvtx(f"seqattn fwd chunk {i} rows {s}:{e}"):
             o_c = bufs.o[:, s:e]
             if o_c.is_contiguous():
                 chunk_fwd(_rows(q, s, e), k, v, o_c, bufs.lse_chunks[i], s, s, scale, st)
@@ -423,7 +429,7 @@ def backward_chunks(q, k, v, d_o, chunk, bufs, scale=None, stream=None, bwd_stre
         st = main if j == 0 else sides[j - 1]
         if before_chunk is not None:
             before_chunk(i, st)
-        with torch.cuda.stream(st):                # as in forward_chunks
+        with torch.cuda.stream(st), _nvtx(f"seqattn bwd chunk {i} rows {s}:{e}"):   # as in forward_chunks
             dq_c = bufs.dq[:, s:e]
             tgt = dq_c if dq_c.is_contiguous() else torch.empty_like(dq_c.contiguous())
             chunk_bwd(_rows(q, s, e), k, v, _rows(bufs.o, s, e), bufs.lse_chunks[i], _rows(d_o, s, e),
