@@ -31,13 +31,14 @@ UNIT = "TFLOP/s"
 FALLBACK_BURST_TFLOPS = 1900.0       # used only when no measured peaks file exists
 FALLBACK_SUSTAINED_TFLOPS = 1700.0
 
-# DRAM traffic (bytes read + written) per backward launch, from the ncu
-# launch list of a workload (average over its chunk launches), keyed by the
-# workload; other workloads report None, and an entry is removed whenever
+# DRAM traffic (bytes read + written) of one backward launch, from a full ncu
+# capture of a mid-sequence chunk of the workload (chunk 7 of 16 for the
+# 32768-token layer: dram__bytes_read.sum + dram__bytes_write.sum), keyed by
+# the workload; other workloads report None, and an entry is removed whenever
 # the kernel changes until it is measured again.
 BWD_TRAFFIC_BYTES_PER_LAUNCH = {
-    # bwd_bf16_kernel<128>, prefix tiles first per head, dK/dV by fp32 reductions
-    "llama3-8b-layer-t32768-c2048": 463.8e6,
+    # bwd_bf16_kernel<128>, dK/dV staged in shared memory and added by TMA reduce-adds
+    "llama3-8b-layer-t32768-c2048": 468.5e6,
 }
 
 
@@ -376,6 +377,7 @@ def run_ours(args, w):
                 "peak_sustained": pk["sustained"], "frac_sustained": bwd_tf / pk["sustained"],
                 "peak_sustained_sm_mhz": pk["sustained_sm_mhz"], "sm_mhz_timed": clock_info.get("sm_mhz"),
                 "traffic": BWD_TRAFFIC_BYTES_PER_LAUNCH.get(w.name),
+                "traffic_source": "ncu full capture of one mid-sequence backward launch (chunk 7 of 16)",
                 "per_launch": f"causal bwd FLOPs 10*Hq*d*pairs(chunk) over the {D} chunk backwards of a "
                               f"step, timed as a phase ({n_bwd} stream(s), fork to join); avg_launch_ms is "
                               f"the phase divided by {D}",

@@ -469,6 +469,9 @@ def test_bf16_32b_layer_t131072_sampled():
 
 
 def test_bf16_partition_sweep_agrees_with_unchunked():
+    """Every chunk size of the 16384-token sweep against the unchunked pass
+    (the whole layer), and the unchunked pass, the smallest and a middle
+    chunk size against the oracle on one key/value group each."""
     w = workloads.WORKLOADS["partition-sweep-t16384"]
     cpu = inputs.layer_inputs(w)
     dev = [x.cuda() for x in cpu]
@@ -481,6 +484,8 @@ def test_bf16_partition_sweep_agrees_with_unchunked():
         got = (bufs.o, binding.gather_lse(bufs), bufs.dq, bufs.dk, bufs.dv)
         for name, a, b in zip(("O", "LSE", "dQ", "dK", "dV"), got, ref_t):
             assert_bf16(f"c={chunk} {name} vs D=1", cpu64(a), cpu64(b))
+        if chunk in (128, 512):
+            _bf16_group_check(w, cpu, bufs, chunk, (0,))
 
 
 def test_bf16_run_to_run_spread_qwen3_layer():
