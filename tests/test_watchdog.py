@@ -34,13 +34,17 @@ def _close(name, got, ref):
     assert rel <= BF16_REL and mx <= BF16_ABS, f"{name}: rel-L2 {rel:.3e} max-abs {mx:.3e}"
 
 
-@pytest.mark.parametrize("d", [128, 64])
-def test_waits_run_out_report_timeout_then_recover(d):
+@pytest.mark.parametrize("d,B,T,Hq,Hkv", [
+    (128, 1, 512, 4, 2),
+    (64, 1, 512, 4, 2),
+    (128, 2, 2304, 32, 8),   # more backward CTAs than SMs, batch 2
+])
+def test_waits_run_out_report_timeout_then_recover(d, B, T, Hq, Hkv):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     build.build()
     lib = binding.load_library()
-    B, T, Hq, Hkv, qs, c = 1, 512, 4, 2, 256, 256
+    qs, c = T - 256, 256
     cpu = [inputs.draw(n, 17, B, T, h, d, torch.bfloat16) for n, h in
            (("q", Hq), ("k", Hkv), ("v", Hkv), ("do", Hq))]
     q, k, v, do = (x.cuda() for x in cpu)
