@@ -186,9 +186,9 @@ seqattn_status seqattn_scale_accum_rows(const seqattn_problem* pb, int64_t row_b
  * the products are summed in float32 and each CTA adds its tile into dw with
  * TMA reduce-adds (atomic per element in L2), so calls that update the same
  * dw may run concurrently on different streams (the order of the fp32
- * additions, and so the last bits of dw, then varies between runs).  Rows of h outside
- * [row_begin, row_end) are read only where they meet a zero of g and must be
- * finite.  Requires batch >= 1, 0 <= row_begin <= row_end <= seq_len,
+ * additions, and so the last bits of dw, then varies between runs).  Rows of
+ * h outside [row_begin, row_end) are read only where they meet a zero of g
+ * and must be finite.  Requires batch >= 1, 0 <= row_begin <= row_end <= seq_len,
  * d_model and n positive multiples of 8, and 16-byte aligned pointers.  No
  * workspace.  Async on `stream`; INVALID_ARG before any launch on a bad
  * argument; row_begin == row_end is a no-op.
