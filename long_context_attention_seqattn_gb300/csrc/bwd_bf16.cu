@@ -109,6 +109,7 @@ struct BwdParams {
   float* dv;
   unsigned int* err;
   long long wait_cycles;
+  int reverse;             // prefix tiles (and batch entries) in descending order
 };
 
 struct BwdBarriers {
@@ -186,14 +187,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- work item: (batch b, kv head g, key tile kt).
   // Per batch entry: first the key tiles that lie wholly before the chunk
   // (all of equal, longest length), key tile fastest within each key/value
-  // head so that a wave shares one group's Q, dO and dq in L2; then the tiles
-  // that reach into the chunk (shorter, decreasing), head fastest, so the
-  // shortest loops form the last wave.
+  // head so that a wave shares one group's Q, dO and dq in L2 (in ascending
+  // or, with p.reverse, descending order of batch entry, head and tile); then
+  // the tiles that reach into the chunk (shorter, decreasing), head fastest,
+  // so the shortest loops form the last wave.
   const int per_b = p.n_ktiles * p.Hkv;
-  const int b = blockIdx.x / per_b;
-  const int idx = blockIdx.x - b * per_b;
+  const int b0 = blockIdx.x / per_b;
+  int idx = blockIdx.x - b0 * per_b;
+  const int b = p.reverse ? p.B - 1 - b0 : b0;
   int g, kt;
   if (idx < p.n_pre * p.Hkv) {
+    if (p.reverse) idx = p.n_pre * p.Hkv - 1 - idx;
     g = idx / p.n_pre;
     kt = idx - g * p.n_pre;
   } else {
@@ -589,6 +593,11 @@ cudaError_t launch_bwd_bf16(const ChunkGeom& g, const Bf16BwdMaps& maps, const f
   p.dv = dv;
   p.err = err;
   p.wait_cycles = g.wait_cycles;
+  // Alternate the sweep direction over the prefix from one chunk to the next
+  // (by the chunk's index in a uniform partition): the prefix rows a call
+  // touched last are then the first the next call touches, while they are
+  // still in L2.  Each dK/dV row still receives exactly one addition per call.
+  p.reverse = static_cast<int>((g.q_start / (g.q_len > 0 ? g.q_len : 1)) & 1);
   const unsigned grid = static_cast<unsigned>(p.n_ktiles) * g.Hkv * g.B;
   return g.d == 64 ? launch_bwd_bf16_d<64>(p, maps, grid, s) : launch_bwd_bf16_d<128>(p, maps, grid, s);
 }

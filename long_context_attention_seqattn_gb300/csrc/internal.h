@@ -57,8 +57,10 @@ cudaError_t launch_bwd_bf16(const ChunkGeom& g, const Bf16BwdMaps& maps, const f
                             float* dq, float* dk, float* dv, unsigned int* err, cudaStream_t s);
 
 // ---- projection weight gradient (tcgen05, G rounded to bf16 in the kernel) -
-// h: bf16 [B, T, d_model], box {64 columns, 64 rows, 1}, 128-byte swizzle;
-// g: fp32 [B, T, n], box {128 columns, 64 rows, 1}, no swizzle;
+// Rows (tokens) per pipeline stage: the height of the h and g boxes.
+constexpr int kWgradStageRows = 64;
+// h: bf16 [B, T, d_model], box {64 columns, kWgradStageRows rows, 1}, 128-byte swizzle;
+// g: fp32 [B, T, n], box {128 columns, kWgradStageRows rows, 1}, no swizzle;
 // dw: fp32 [1, d_model, n], box {128 columns, 32 rows, 1}, no swizzle (the
 // target of the epilogue's reduce-adds).
 struct WgradMaps {

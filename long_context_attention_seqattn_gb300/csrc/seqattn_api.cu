@@ -333,8 +333,8 @@ seqattn_status seqattn_proj_wgrad(int32_t batch, int64_t seq_len, int64_t row_be
   cudaError_t e = error_word(&err);
   if (e != cudaSuccess) return cuda_fail(e, "error word");
   WgradMaps maps;
-  if (!make_map_btc(&maps.h, h, batch, seq_len, d_model, false, 64, 64) ||
-      !make_map_btc(&maps.g, g, batch, seq_len, n, true, 128, 64) ||
+  if (!make_map_btc(&maps.h, h, batch, seq_len, d_model, false, 64, kWgradStageRows) ||
+      !make_map_btc(&maps.g, g, batch, seq_len, n, true, 128, kWgradStageRows) ||
       !make_map_btc(&maps.dw, dw, 1, d_model, n, true, 128, 32))
     return fail(SEQATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for h, g or dw");
   e = launch_wgrad_bf16(maps, batch, row_begin, row_end, d_model, n, err,
