@@ -37,8 +37,9 @@ FALLBACK_SUSTAINED_TFLOPS = 1700.0
 # the workload; other workloads report None, and an entry is removed whenever
 # the kernel changes until it is measured again.
 BWD_TRAFFIC_BYTES_PER_LAUNCH = {
-    # bwd_bf16_kernel<128>, dK/dV staged in shared memory and added by TMA reduce-adds
-    "llama3-8b-layer-t32768-c2048": 468.5e6,
+    # bwd_bf16_kernel<128>: dK/dV added by TMA reduce-adds, prefix swept in
+    # alternating direction from chunk to chunk (chunk 7 runs it descending)
+    "llama3-8b-layer-t32768-c2048": 468.9e6,
 }
 
 
