@@ -204,14 +204,17 @@ def test_bf16_ragged_shapes(B, T, Hq, Hkv, d, chunk):
     _check_bf16_layer(B, T, Hq, Hkv, d, chunk, seed=12)
 
 
-def test_bf16_truncated_prefix_single_chunk():
+@pytest.mark.parametrize("qs,c,p", [
+    (300, 130, 171),   # chunk index q_start / q_len = 2: prefix tiles swept ascending
+    (390, 130, 171),   # index 3: swept descending, batch entries in reverse order
+])
+def test_bf16_truncated_prefix_single_chunk(qs, c, p):
     """prefix_len < q_start: keys [q_start - prefix_len, q_start + r] only,
     with every bound off the tile grid; accumulator rows outside the window
     stay zero."""
     B, T, Hq, Hkv, d = 2, 600, 4, 2, 128
     cpu = small_inputs(B, T, Hq, Hkv, d, "bf16", 23)
     q, k, v, do = (x.cuda() for x in cpu)
-    qs, c, p = 300, 130, 171
     lse = torch.empty((B, Hq, c), device="cuda")
     o_c = torch.empty((B, c, Hq, d), dtype=torch.bfloat16, device="cuda")
     dq_c = torch.empty((B, c, Hq, d), device="cuda")
